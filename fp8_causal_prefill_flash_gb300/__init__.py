@@ -1,1 +1,201 @@
-"""GB300-native FP8 / BF16 causal prefill FlashAttention (placeholder binding)."""
+"""GB300-native FP8 / BF16 causal prefill FlashAttention.
+
+A thin binding over the C ABI of ``libfp8attn.so`` (``include/fp8attn.h``).
+It only marshals torch tensors into pointers, sizes and the current CUDA
+stream: every step of the computation runs in the library's sm_103a kernels.
+If the library has not been built the calls raise; there is no CPU path.
+
+Entry points (same names as the C ABI):
+
+* ``attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v)`` -- Lean-P
+* ``attn_fwd_fp8_exact(...)`` -- exact-softmax FP8 ablation
+* ``attn_fwd_bf16(q, k, v)`` -- exact-softmax BF16
+* ``attn_fwd_ex(variant, ...)`` -- fp32 output, explicit scale, status word
+
+Tensors are [B, S, H, D] contiguous CUDA tensors: uint8 / float8_e4m3fn codes
+for FP8 (descales are one-element float32 CUDA tensors), bfloat16 for BF16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ARCH = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+
+ATTN_VARIANT_LEANP = 0
+ATTN_VARIANT_EXACT_FP8 = 1
+ATTN_VARIANT_BF16 = 2
+ATTN_OUT_BF16 = 0
+ATTN_OUT_F32 = 1
+ATTN_FLAG_TEST_STALL_LOADS = 1
+
+HEADER = os.path.join(_build.ROOT, "include", "fp8attn.h")
+LIBRARY_PATH = _build.SO
+
+_lib = None
+_lock = threading.Lock()
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile libfp8attn.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def load_library():
+    """Load libfp8attn.so; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIBRARY_PATH):
+            raise RuntimeError(
+                f"{LIBRARY_PATH} is missing: build it with fp8_causal_prefill_flash_gb300.build()")
+        lib = ctypes.CDLL(LIBRARY_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fp8_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+        lib.attn_fwd_fp8.argtypes = fp8_args
+        lib.attn_fwd_fp8_exact.argtypes = fp8_args
+        lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+        lib.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
+                                    vp, vp]
+        for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
+                     "attn_launches_per_call", "attn_api_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/fp8attn.h declares."""
+    with open(HEADER) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", text, re.M)))
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check_qkv(q, k, v, fp8: bool):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, S, H, D] tensor")
+        if fp8 and t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn)")
+        if not fp8 and t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+    B, S, Hq, Dqk = q.shape
+    _, _, Hkv, _ = k.shape
+    Dv = v.shape[3]
+    return B, Hq, Hkv, S, Dqk, Dv
+
+
+def _check_descale(name, t):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float32 or t.numel() < 1:
+        raise TypeError(f"{name} must be a float32 CUDA tensor with one element")
+
+
+def _out(out, q, Dv, dtype):
+    B, S, Hq, _ = q.shape
+    if out is None:
+        return torch.empty((B, S, Hq, Dv), dtype=dtype, device=q.device)
+    if out.shape != (B, S, Hq, Dv) or out.dtype != dtype or not out.is_contiguous():
+        raise ValueError("out has the wrong shape, dtype or layout")
+    return out
+
+
+def _raise(status, what):
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, out=None, causal=True):
+    """Lean-P FP8 causal prefill attention; returns bf16 [B, S, Hq, Dv]."""
+    lib = load_library()
+    B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, True)
+    for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        _check_descale(n, t)
+    out = _out(out, q, Dv, torch.bfloat16)
+    st = lib.attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                          _ptr(descale_v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv, int(bool(causal)),
+                          _stream_handle())
+    _raise(st, "attn_fwd_fp8")
+    return out
+
+
+def attn_fwd_fp8_exact(q, k, v, descale_q, descale_k, descale_v, out=None, causal=True):
+    """Exact-softmax FP8 ablation; returns bf16 [B, S, Hq, Dv]."""
+    lib = load_library()
+    B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, True)
+    for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        _check_descale(n, t)
+    out = _out(out, q, Dv, torch.bfloat16)
+    st = lib.attn_fwd_fp8_exact(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                                _ptr(descale_v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv,
+                                int(bool(causal)), _stream_handle())
+    _raise(st, "attn_fwd_fp8_exact")
+    return out
+
+
+def attn_fwd_bf16(q, k, v, out=None, causal=True):
+    """Exact-softmax BF16 causal prefill attention; returns bf16 [B, S, Hq, Dv]."""
+    lib = load_library()
+    B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, False)
+    out = _out(out, q, Dv, torch.bfloat16)
+    st = lib.attn_fwd_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv,
+                           int(bool(causal)), _stream_handle())
+    _raise(st, "attn_fwd_bf16")
+    return out
+
+
+def attn_fwd_ex(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None, out=None,
+                out_dtype=ATTN_OUT_F32, softmax_scale=0.0, flags=0, dev_status=None,
+                causal=True, raise_on_error=True):
+    """Extended call: any variant, fp32 or bf16 output, explicit softmax scale,
+    test flags and an optional int32 CUDA status tensor (zeroed by the caller)."""
+    lib = load_library()
+    fp8 = variant != ATTN_VARIANT_BF16
+    B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, fp8)
+    if fp8:
+        for n, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+            _check_descale(n, t)
+    dtype = torch.float32 if out_dtype == ATTN_OUT_F32 else torch.bfloat16
+    out = _out(out, q, Dv, dtype)
+    st = lib.attn_fwd_ex(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(descale_q),
+                         _ptr(descale_k), _ptr(descale_v), _ptr(out), int(out_dtype), B, Hq, Hkv,
+                         S, Dqk, Dv, int(bool(causal)), float(softmax_scale), int(flags),
+                         _ptr(dev_status), _stream_handle())
+    if raise_on_error:
+        _raise(st, "attn_fwd_ex")
+        return out
+    return out, st

@@ -1,0 +1,240 @@
+// api.cu -- the C ABI of libfp8attn.so (declared in include/fp8attn.h):
+// argument checks, TMA tensor maps, and the launch of the persistent kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fp8attn.h"
+#include "attn_fwd.cuh"
+
+namespace {
+
+using fa8::KParams;
+using fa8::Maps;
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;      // 4 s per wait
+constexpr unsigned long long kTestWaitLimitNs = 200000000ull;   // 0.2 s (stall test)
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  std::atomic<int> state{0};  // 0 unknown, 1 sm_103, 2 other
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Checks the current device once: sm_103 and its SM count.
+int device_check(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  DeviceInfo& d = g_dev[dev];
+  int st = d.state.load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    st = d.state.load(std::memory_order_relaxed);
+    if (st == 0) {
+      int major = 0, minor = 0, n = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+      d.sms = n;
+      st = (major == 10 && minor == 3) ? 1 : 2;
+      d.state.store(st, std::memory_order_release);
+    }
+  }
+  if (st != 1) return ATTN_ERR_ARCH;
+  *sms = d.sms;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D tensor map over a BSHD tensor: dims (D, H, S, B) innermost first; the
+// box is `box_inner` elements of D, one head, 128 rows of S, one batch.
+int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int D, int H,
+             int S, int B, int box_inner, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return ATTN_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize,
+                           (cuuint64_t)S * H * D * esize};
+  cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int V, int DQK>
+int launch(const Maps& maps, const KParams& p, int sms, cudaStream_t stream) {
+  using C = fa8::Cfg<V, DQK>;
+  auto kern = fa8::attn_fwd_kernel<V, DQK>;
+  // Per-device opt-in to the large dynamic shared memory carve-out.
+  static std::atomic<unsigned long long> done_mask[1] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(done_mask[0].load(std::memory_order_acquire) & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    done_mask[0].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  const int grid = p.n_items < sms ? p.n_items : sms;
+  kern<<<grid, fa8::kThreads, C::kSmemAlloc, stream>>>(maps, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int run(int variant, const void* q, const void* k, const void* v, const float* dq, const float* dk,
+        const float* dv, void* out, int out_dtype, int B, int Hq, int Hkv, int S, int Dqk, int Dv,
+        int causal, float softmax_scale, int flags, int* dev_status, void* stream) {
+  // ---- argument checks (before anything touches the device)
+  if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_BF16) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return ATTN_ERR_INVALID_ARG;
+  const bool fp8 = variant != ATTN_VARIANT_BF16;
+  if (fp8 && (!dq || !dk || !dv)) return ATTN_ERR_INVALID_ARG;
+  if (fp8 && ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+               reinterpret_cast<uintptr_t>(dv)) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Dqk < 1 || Dv < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return ATTN_ERR_INVALID_ARG;
+  if ((flags & ATTN_FLAG_TEST_STALL_LOADS) && !dev_status) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAG_TEST_STALL_LOADS) return ATTN_ERR_INVALID_ARG;
+  if (causal != 1) return ATTN_ERR_UNSUPPORTED;
+  if (Dv != 128) return ATTN_ERR_UNSUPPORTED;
+  if (fp8 ? (Dqk != 128 && Dqk != 192) : (Dqk != 128)) return ATTN_ERR_UNSUPPORTED;
+  // index ranges: the kernel's int arithmetic covers B*Hq*ceil(S/256) items
+  const long long n_qblocks = (S + 255) / 256;
+  const long long n_items = (long long)B * Hq * n_qblocks;
+  if (n_items > (1ll << 30) || (long long)B * S > (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+
+  int sms = 0;
+  int st = device_check(&sms);
+  if (st != ATTN_OK) return st;
+
+  KParams p;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S = S;
+  p.group = Hq / Hkv;
+  p.n_qblocks = (int)n_qblocks;
+  p.n_kv_tiles = (S + 127) / 128;
+  p.n_items = (int)n_items;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / std::sqrt((float)Dqk);
+  p.out = out;
+  p.out_f32 = out_dtype == ATTN_OUT_F32;
+  p.status = dev_status;
+  p.flags = flags;
+  p.wait_limit_ns = (flags & ATTN_FLAG_TEST_STALL_LOADS) ? kTestWaitLimitNs : kWaitLimitNs;
+
+  Maps maps;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int es = fp8 ? 1 : 2;
+  const int inner = 128 / es;  // elements per 128-byte panel
+  if ((st = make_map(&maps.q128, q, dt, es, Dqk, Hq, S, B, inner, CU_TENSOR_MAP_SWIZZLE_128B)))
+    return st;
+  if ((st = make_map(&maps.k128, k, dt, es, Dqk, Hkv, S, B, inner, CU_TENSOR_MAP_SWIZZLE_128B)))
+    return st;
+  if ((st = make_map(&maps.v, v, dt, es, Dv, Hkv, S, B, inner, CU_TENSOR_MAP_SWIZZLE_128B)))
+    return st;
+  if (Dqk == 192) {
+    if ((st = make_map(&maps.q64, q, dt, es, Dqk, Hq, S, B, 64, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+    if ((st = make_map(&maps.k64, k, dt, es, Dqk, Hkv, S, B, 64, CU_TENSOR_MAP_SWIZZLE_64B)))
+      return st;
+  } else {
+    maps.q64 = maps.q128;
+    maps.k64 = maps.k128;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (variant) {
+    case ATTN_VARIANT_LEANP:
+      return Dqk == 128 ? launch<fa8::kLeanP, 128>(maps, p, sms, s)
+                        : launch<fa8::kLeanP, 192>(maps, p, sms, s);
+    case ATTN_VARIANT_EXACT_FP8:
+      return Dqk == 128 ? launch<fa8::kExactFp8, 128>(maps, p, sms, s)
+                        : launch<fa8::kExactFp8, 192>(maps, p, sms, s);
+    default:
+      return launch<fa8::kBf16, 128>(maps, p, sms, s);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* descale_q,
+                 const float* descale_k, const float* descale_v, void* out, int B, int Hq,
+                 int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
+  return run(ATTN_VARIANT_LEANP, q, k, v, descale_q, descale_k, descale_v, out, ATTN_OUT_BF16, B,
+             Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+}
+
+int attn_fwd_fp8_exact(const void* q, const void* k, const void* v, const float* descale_q,
+                       const float* descale_k, const float* descale_v, void* out, int B,
+                       int Hq, int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
+  return run(ATTN_VARIANT_EXACT_FP8, q, k, v, descale_q, descale_k, descale_v, out,
+             ATTN_OUT_BF16, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+}
+
+int attn_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                  int S, int Dqk, int Dv, int causal, void* stream) {
+  return run(ATTN_VARIANT_BF16, q, k, v, nullptr, nullptr, nullptr, out, ATTN_OUT_BF16, B, Hq,
+             Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+}
+
+int attn_fwd_ex(int variant, const void* q, const void* k, const void* v, const float* descale_q,
+                const float* descale_k, const float* descale_v, void* out, int out_dtype, int B,
+                int Hq, int Hkv, int S, int Dqk, int Dv, int causal, float softmax_scale,
+                int flags, int* dev_status, void* stream) {
+  return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, B, Hq, Hkv, S,
+             Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_launches_per_call(void) { return 1; }
+
+int attn_api_version(void) { return FP8ATTN_API_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,649 @@
+// attn_fwd.cuh -- warp-specialised causal prefill attention for GB300 (sm_103a).
+//
+// One persistent CTA per SM.  A work item is (batch b, query head h, query
+// block qb) with two 128-row query tiles (rows 256*qb .. 256*qb+255); the two
+// tiles share every K/V tile that TMA brings in.  Roles (12 warps):
+//   warps 0-3   softmax warpgroup 0 (query tile 0, thread = row)
+//   warps 4-7   softmax warpgroup 1 (query tile 1)
+//   warp  8     TMA producer: Q tiles once per item, K/V tiles through a ring
+//   warp  9     MMA issuer (one thread) and tensor-memory owner
+//   warps 10-11 idle (complete the last warpgroup)
+// Tensor memory (512 columns x 128 lanes of 32-bit):
+//   [  0,128) S0 / P0    [128,256) S1 / P1    [256,384) O0    [384,512) O1
+// S_t = Q_t K_j^T lands in its region; the softmax warpgroup reads it, then
+// writes the probabilities P_t (FP8 codes: 32 columns, BF16: 64 columns) and
+// the block-scale factors into the same region, where the P.V MMA reads them.
+// The MMA issue order per key tile j is PV0(j), QK0(j+1), PV1(j), QK1(j+1),
+// so the softmax of one query tile overlaps the tensor-core work of the other
+// ("two-wave ping-pong" in "Zyphra ZYFA: FP8 FlashAttention for AMD MI355X",
+// "How does ZYFA work?", re-expressed with asynchronous tcgen05 MMAs whose
+// completion mbarriers track, instead of instruction ordering).
+//
+// Probability policies (softmax warpgroups):
+//   kLeanP     one multiply-add per probability rounded toward minus infinity
+//              into the magic range [2^23, 2^24), whose low byte is the e4m3
+//              code ("Lean P: one multiply-add instead of an exponential"); a
+//              power-of-two scale per 64-key block enters the P.V MMA as a
+//              UE8M0 block-scale factor and the row sum adds the rounded
+//              probabilities ("Per-block scaling and a rounded row sum").
+//   kExactFp8  p = 2^(x - m) on the MUFU, rounded to e4m3, unrounded row sum.
+//   kBf16      as kExactFp8 with bf16 operands and probabilities.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace fa8 {
+
+enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2 };
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kDV = 128;  // value head dim
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+
+// Lean-P constants.  T = 7 headroom binades: the largest probability of each
+// 64-key block gets a code in [C-8, C], C = 8*(7+T) = 112 (the code of 2^T).
+constexpr int kLeanT = 7;
+constexpr float kLeanC = 112.0f;
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: floats in [2^23, 2^24) have unit spacing
+// A row's reference binade is only raised when a block exponent exceeds it
+// by more than this many binades (all rescales are exact powers of two).
+constexpr float kLazyBinades = 8.0f;
+
+template <int V, int DQK>
+struct Cfg {
+  static constexpr bool kFp8 = V != kBf16;
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kRowBytes = DQK * kElem;             // bytes of one Q/K row
+  static constexpr int kFullPanels = kRowBytes / 128;       // 128-byte swizzled panels
+  static constexpr int kTailBytes = kRowBytes % 128;        // 0 or 64 (MLA shape)
+  static constexpr int kPanelBytes = 128 * 128;             // 128 rows x 128 bytes
+  static constexpr int kTailPanelBytes = 128 * kTailBytes;  // 128 rows x 64 bytes
+  static constexpr int kQkTileBytes = kFullPanels * kPanelBytes + kTailPanelBytes;
+  static constexpr int kVTileBytes = kBN * kDV * kElem;
+  static constexpr int kVPanels = kDV * kElem / 128;
+  static constexpr int kStages = kFp8 ? (DQK == 128 ? 4 : 3) : 2;
+  static constexpr int kSmemQ = 0;
+  static constexpr int kSmemK = 2 * kQkTileBytes;
+  static constexpr int kSmemV = kSmemK + kStages * kQkTileBytes;
+  static constexpr int kSmemBytes = kSmemV + kStages * kVTileBytes;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+  static constexpr int kQkSteps = kRowBytes / 32;       // one MMA per 32 bytes of K
+  static constexpr int kPvSteps = kFp8 ? 4 : 8;         // 128 keys / (32 fp8 or 16 bf16)
+  static constexpr int kPCols = kFp8 ? 32 : 64;         // TMEM columns of P per tile
+  static_assert(kTailBytes == 0 || kTailBytes == 64, "row bytes must be 128*n or 128*n+64");
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+};
+
+struct KParams {
+  int B, Hq, Hkv, S;
+  int group;         // Hq / Hkv
+  int n_qblocks;     // ceil(S / 256)
+  int n_kv_tiles;    // ceil(S / 128)
+  int n_items;       // B * Hq * n_qblocks
+  const float* dq;   // device descales (FP8 only)
+  const float* dk;
+  const float* dv;
+  float scale;       // softmax scale
+  void* out;
+  int out_f32;
+  int* status;       // optional device status word
+  int flags;
+  unsigned long long wait_limit_ns;
+};
+
+struct Maps {
+  CUtensorMap q128, k128, v;  // 128-byte panels (SW128)
+  CUtensorMap q64, k64;       // 64-byte tail panel of the MLA shape (SW64)
+};
+
+// Items are visited longest first (query block descending); CTA c takes the
+// c-th item of each round of gridDim.x items, alternating direction every
+// round, so that every CTA gets a similar share of causal work.
+__device__ __forceinline__ int item_at(int round, int n_items) {
+  const int G = gridDim.x;
+  const int pos = round * G + ((round & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return pos < n_items ? pos : -1;
+}
+
+__device__ __forceinline__ void decode_item(const KParams& p, int idx, int& b, int& h, int& qb) {
+  const int per_qb = p.B * p.Hq;
+  qb = p.n_qblocks - 1 - idx / per_qb;
+  const int r = idx % per_qb;
+  b = r / p.Hq;
+  h = r % p.Hq;
+}
+
+// Number of key tiles query tile t of block qb needs (keys < min(S, last row + 1)).
+__device__ __forceinline__ int kv_tiles_for(const KParams& p, int qb, int t) {
+  const int need = 2 * qb + t + 1;
+  return need < p.n_kv_tiles ? need : p.n_kv_tiles;
+}
+
+struct __align__(8) Barriers {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// --------------------------------------------------------------------------
+// Producer warp: TMA loads.
+// --------------------------------------------------------------------------
+template <int V, int DQK>
+__device__ __forceinline__ void load_qk_tile(uint8_t* dst, const Maps& m, bool is_q,
+                                             uint64_t* bar, int head, int row, int b) {
+  using C = Cfg<V, DQK>;
+  const CUtensorMap* full = is_q ? &m.q128 : &m.k128;
+#pragma unroll
+  for (int pnl = 0; pnl < C::kFullPanels; ++pnl)
+    tma_load_4d(dst + pnl * C::kPanelBytes, full, bar, pnl * (128 / C::kElem), head, row, b);
+  if constexpr (C::kTailBytes) {
+    const CUtensorMap* tail = is_q ? &m.q64 : &m.k64;
+    tma_load_4d(dst + C::kFullPanels * C::kPanelBytes, tail, bar,
+                C::kFullPanels * (128 / C::kElem), head, row, b);
+  }
+}
+
+template <int V, int DQK>
+__device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Barriers& bars) {
+  using C = Cfg<V, DQK>;
+  if (!elect_one()) return;
+  if (p.flags & 1) return;  // test hook: issue nothing, every consumer wait expires
+  prefetch_tmap(&m.q128);
+  prefetch_tmap(&m.k128);
+  prefetch_tmap(&m.v);
+  volatile int* ab = &bars.abort_flag;
+  uint32_t kv_it = 0, q_it = 0, nk = 0, nv = 0;
+  for (int round = 0;; ++round) {
+    const int idx = item_at(round, p.n_items);
+    if (idx < 0) break;
+    int b, h, qb;
+    decode_item(p, idx, b, h, qb);
+    const int g = h / p.group;
+    if (!mbar_wait(&bars.q_empty, (q_it & 1) ^ 1, ab, p.wait_limit_ns)) break;
+    mbar_arrive_expect_tx(&bars.q_full, 2 * C::kQkTileBytes);
+    load_qk_tile<V, DQK>(smem + C::kSmemQ, m, true, &bars.q_full, h, qb * 256, b);
+    load_qk_tile<V, DQK>(smem + C::kSmemQ + C::kQkTileBytes, m, true, &bars.q_full, h,
+                         qb * 256 + 128, b);
+    ++q_it;
+    const int nkv = kv_tiles_for(p, qb, 1);
+    for (int j = 0; j < nkv; ++j, ++kv_it) {
+      const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
+      if (!mbar_wait(&bars.k_empty[st], ph ^ 1, ab, p.wait_limit_ns)) break;
+      mbar_arrive_expect_tx(&bars.k_full[st], C::kQkTileBytes);
+      load_qk_tile<V, DQK>(smem + C::kSmemK + st * C::kQkTileBytes, m, false, &bars.k_full[st], g,
+                           j * kBN, b);
+      ++nk;
+      if (!mbar_wait(&bars.v_empty[st], ph ^ 1, ab, p.wait_limit_ns)) break;
+      ++nv;
+      mbar_arrive_expect_tx(&bars.v_full[st], C::kVTileBytes);
+#pragma unroll
+      for (int pnl = 0; pnl < C::kVPanels; ++pnl)
+        tma_load_4d(smem + C::kSmemV + st * C::kVTileBytes + pnl * C::kPanelBytes, &m.v,
+                    &bars.v_full[st], pnl * (128 / C::kElem), g, j * kBN, b);
+    }
+    if (*ab) break;
+  }
+  if (*ab) {
+    // Before the CTA may exit, every copy this thread started must have landed.
+    constexpr uint64_t kDrainNs = 50000000ull;
+    volatile int dummy = 0;
+    for (uint32_t i = nk > (uint32_t)C::kStages ? nk - C::kStages : 0; i < nk; ++i)
+      mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
+    for (uint32_t i = nv > (uint32_t)C::kStages ? nv - C::kStages : 0; i < nv; ++i)
+      mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
+    if (q_it) mbar_wait(&bars.q_full, (q_it - 1) & 1, &dummy, kDrainNs);
+  }
+}
+
+// --------------------------------------------------------------------------
+// MMA warp: one thread issues every tcgen05.mma.
+// --------------------------------------------------------------------------
+template <int V, int DQK>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, int t, uint32_t k_off) {
+  using C = Cfg<V, DQK>;
+  constexpr uint32_t idesc = idesc_f32acc(128, 128, C::kFp8 ? 0 : 1, C::kFp8 ? 0 : 1, 0, 0);
+  const uint32_t q_off = C::kSmemQ + t * C::kQkTileBytes;
+#pragma unroll
+  for (int k = 0; k < C::kQkSteps; ++k) {
+    const int byte = 32 * k;
+    const int pnl = byte / 128;
+    uint64_t a, bdesc;
+    if (pnl < C::kFullPanels) {
+      const uint32_t o = pnl * C::kPanelBytes + (byte % 128);
+      a = smem_desc(smem_base + q_off + o, 16, 1024, kSwizzle128B);
+      bdesc = smem_desc(smem_base + k_off + o, 16, 1024, kSwizzle128B);
+    } else {
+      const uint32_t o = C::kFullPanels * C::kPanelBytes + (byte % 128);
+      a = smem_desc(smem_base + q_off + o, 16, 512, 4);
+      bdesc = smem_desc(smem_base + k_off + o, 16, 512, 4);
+    }
+    if constexpr (C::kFp8)
+      mma_f8_ss(tmem + t * 128, a, bdesc, idesc, k > 0);
+    else
+      mma_f16_ss(tmem + t * 128, a, bdesc, idesc, k > 0);
+  }
+}
+
+template <int V, int DQK>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int t, uint32_t v_off,
+                                         bool accumulate) {
+  using C = Cfg<V, DQK>;
+  const uint32_t d = tmem + 256 + t * 128;
+  const uint32_t a = tmem + t * 128;  // P at the start of the S region
+  if constexpr (C::kFp8) {
+    const uint32_t sfa = tmem + t * 128 + 32;  // + lane quadrant (per the MMA's read pattern)
+    const uint32_t sfb = tmem + t * 128 + 36;
+#pragma unroll
+    for (int k = 0; k < C::kPvSteps; ++k) {
+      const uint64_t bdesc = smem_desc(smem_base + v_off + 4096 * k, 1024, 1024, kSwizzle128B);
+      mma_mx8_ts(d, a + 8 * k, bdesc, idesc_mx(128, 128, 0, 0, 0, 1, k, k), sfa, sfb,
+                 accumulate || k > 0);
+    }
+  } else {
+    constexpr uint32_t idesc = idesc_f32acc(128, 128, 1, 1, 0, 1);
+#pragma unroll
+    for (int k = 0; k < C::kPvSteps; ++k) {
+      const uint64_t bdesc =
+          smem_desc(smem_base + v_off + 2048 * k, C::kPanelBytes, 1024, kSwizzle128B);
+      mma_f16_ts(d, a + 8 * k, bdesc, idesc, accumulate || k > 0);
+    }
+  }
+}
+
+template <int V, int DQK>
+__device__ void mma_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
+  using C = Cfg<V, DQK>;
+  if (lane_id() != 0) return;
+  volatile int* ab = &bars.abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+  uint32_t kv_it = 0, q_it = 0;
+  uint32_t p_cnt[2] = {0, 0}, items_t[2] = {0, 0};
+  for (int round = 0;; ++round) {
+    const int idx = item_at(round, p.n_items);
+    if (idx < 0) break;
+    int b, h, qb;
+    decode_item(p, idx, b, h, qb);
+    const int nkv0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
+    if (!mbar_wait(&bars.q_full, q_it & 1, ab, lim)) return;
+    ++q_it;
+    tc_fence_after();
+    // prologue: S_t(0) for both tiles
+    {
+      const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
+      if (!mbar_wait(&bars.k_full[st], ph, ab, lim)) return;
+      tc_fence_after();
+      const uint32_t k_off = smem_base + C::kSmemK + st * C::kQkTileBytes - smem_base;
+      for (int t = 0; t < 2; ++t) {
+        if (0 < (t ? nkv : nkv0)) {
+          issue_qk<V, DQK>(tmem, smem_base, t, k_off);
+          tc_commit(&bars.s_full[t]);
+        }
+      }
+      tc_commit(&bars.k_empty[st]);
+      if (nkv == 1) tc_commit(&bars.q_empty);
+    }
+    for (int j = 0; j < nkv; ++j) {
+      const uint32_t it = kv_it + j;
+      const uint32_t st = it % C::kStages, ph = (it / C::kStages) & 1;
+      const uint32_t stn = (it + 1) % C::kStages, phn = ((it + 1) / C::kStages) & 1;
+      const bool has_next = j + 1 < nkv;
+      bool next_k_ready = false;
+      if (!mbar_wait(&bars.v_full[st], ph, ab, lim)) return;
+      tc_fence_after();
+      const uint32_t v_off = C::kSmemV + st * C::kVTileBytes;
+      for (int t = 0; t < 2; ++t) {
+        const int nk_t = t ? nkv : nkv0;
+        if (j < nk_t) {
+          if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
+          ++p_cnt[t];
+          if (j == 0) {
+            // the previous item's epilogue must have read O_t
+            if (!mbar_wait(&bars.o_free[t], (items_t[t] & 1) ^ 1, ab, lim)) return;
+            ++items_t[t];
+          }
+          tc_fence_after();
+          issue_pv<V, DQK>(tmem, smem_base, t, v_off, j > 0);
+          tc_commit(&bars.o_done[t]);
+        }
+        if (has_next && j + 1 < nk_t) {
+          if (!next_k_ready) {
+            if (!mbar_wait(&bars.k_full[stn], phn, ab, lim)) return;
+            tc_fence_after();
+            next_k_ready = true;
+          }
+          issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + stn * C::kQkTileBytes);
+          tc_commit(&bars.s_full[t]);
+        }
+      }
+      tc_commit(&bars.v_empty[st]);
+      if (has_next) {
+        tc_commit(&bars.k_empty[stn]);
+        if (j + 2 == nkv) tc_commit(&bars.q_empty);
+      }
+    }
+    kv_it += nkv;
+  }
+}
+
+// --------------------------------------------------------------------------
+// Softmax warpgroups.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack4_low_bytes(float a, float b, float c, float d) {
+  const uint32_t ab = prmt(__float_as_uint(a), __float_as_uint(b), 0x0040);
+  const uint32_t cd = prmt(__float_as_uint(c), __float_as_uint(d), 0x0040);
+  return prmt(ab, cd, 0x5410);
+}
+
+// Sum of the e4m3 values of the four codes in `w`, added to acc0/acc1 in fp32
+// (pairs are added exactly-representable in f16 first).
+__device__ __forceinline__ void add_codes(uint32_t w, float& acc0, float& acc1) {
+  const uint32_t h01 = e4m3x2_to_f16x2(w & 0xFFFFu);
+  const uint32_t h23 = e4m3x2_to_f16x2(w >> 16);
+  uint32_t hs;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hs) : "r"(h01), "r"(h23));
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.f16 %0, lo, %0;\n"
+      " add.rn.f32.f16 %1, hi, %1;\n}\n"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(hs));
+}
+
+__device__ __forceinline__ float pow2i(int e) {  // exact 2^e for e in [-126, 127]
+  return __int_as_float((e + 127) << 23);
+}
+
+// Every lane waits; the warp proceeds only if all lanes saw the phase
+// complete, so warp-collective tcgen05 instructions never run with part of
+// the warp gone on the abort path.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* ab,
+                                          uint64_t lim) {
+  const bool ok = mbar_wait(bar, parity, ab, lim);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int V, int DQK>
+__device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, int t) {
+  using C = Cfg<V, DQK>;
+  volatile int* ab = &bars.abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+  const uint32_t quad = warp_id() & 3;
+  const int r = (int)(quad * 32 + lane_id());  // row within the query tile
+  const uint32_t lane_base = (quad * 32) << 16;
+  const uint32_t s_col = tmem + lane_base + t * 128;
+  const uint32_t o_col = tmem + lane_base + 256 + t * 128;
+  float dqk = 1.0f, dvv = 1.0f;
+  if constexpr (C::kFp8) {
+    dqk = __ldg(p.dq) * __ldg(p.dk);
+    dvv = __ldg(p.dv);
+  }
+  const float log2e = 1.4426950408889634f;
+  const float lam = log2e * p.scale * dqk;  // log2 units per unit of s
+  const float lam8 = 8.0f * lam;            // Lean-P code units per unit of s
+  uint32_t s_cnt = 0, o_cnt = 0;
+
+  for (int round = 0;; ++round) {
+    const int idx = item_at(round, p.n_items);
+    if (idx < 0) break;
+    int b, h, qb;
+    decode_item(p, idx, b, h, qb);
+    const int nk = kv_tiles_for(p, qb, t);
+    const int row = qb * 256 + t * 128 + r;
+    float l = 0.0f;
+    float ref = 0.0f;  // Lean-P: reference binade; exact paths: running max (log2 units)
+    bool have_ref = false;
+    for (int j = 0; j < nk; ++j) {
+      if (!warp_wait(&bars.s_full[t], s_cnt & 1, ab, lim)) return;
+      ++s_cnt;
+      tc_fence_after();
+      uint32_t s[128];
+      {
+        uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[0]);
+        uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32]);
+        uint32_t (&s2)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[64]);
+        uint32_t (&s3)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[96]);
+        tmem_ld32x2_wait(s_col, s_col + 32, s0, s1);
+        tmem_ld32x2_wait(s_col + 64, s_col + 96, s2, s3);
+      }
+      const int key0 = j * kBN;
+      if (key0 + kBN - 1 > row) {  // diagonal (or ragged) tile: mask keys after the row
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (key0 + c > row) s[c] = __float_as_uint(-INFINITY);
+      }
+      bool rescale = false;
+      float alpha = 1.0f;
+      uint32_t pw[C::kPCols];
+      if constexpr (V == kLeanP) {
+        // block maxima of the two 64-key blocks
+        float m0 = __uint_as_float(s[0]), m1 = __uint_as_float(s[64]);
+#pragma unroll
+        for (int c = 1; c < 63; c += 2) {
+          m0 = fmax3(m0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          m1 = fmax3(m1, __uint_as_float(s[64 + c]), __uint_as_float(s[64 + c + 1]));
+        }
+        m0 = fmaxf(m0, __uint_as_float(s[63]));
+        m1 = fmaxf(m1, __uint_as_float(s[127]));
+        // block exponents e = ceil(lam*max): the block maximum lands in (2^(T-1), 2^T]
+        const float e0 = ceilf(m0 * lam8 * 0.125f), e1 = ceilf(m1 * lam8 * 0.125f);
+        const float emax = fmaxf(e0, e1);
+        if (!have_ref) {
+          ref = emax;
+          have_ref = true;
+        } else if (emax > ref + kLazyBinades) {
+          const float d = ref - emax;
+          alpha = d < -126.0f ? 0.0f : pow2i((int)d);
+          ref = emax;
+          rescale = true;
+        }
+        // UE8M0 scale of each block: 2^(e - T - ref), clamped to the format
+        const bool v0 = e0 > -INFINITY, v1 = e1 > -INFINITY;
+        const int x0 = v0 ? max(min((int)(e0 - ref) - kLeanT + 127, 254), 0) : 0;
+        const int x1 = v1 ? max(min((int)(e1 - ref) - kLeanT + 127, 254), 0) : 0;
+        // FMA bias per block: magic - 8e + C (exact integers in fp32)
+        const float B0 = v0 ? kMagic - 8.0f * e0 + kLeanC : kMagic;
+        const float B1 = v1 ? kMagic - 8.0f * e1 + kLeanC : kMagic;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 32; ++w) {
+          const float Bb = w < 16 ? B0 : B1;
+          float y[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            y[i] = fmaxf(fma_rm(__uint_as_float(s[4 * w + i]), lam8, Bb), kMagic);
+          pw[w] = pack4_low_bytes(y[0], y[1], y[2], y[3]);
+          if (w < 16)
+            add_codes(pw[w], a0, a1);
+          else
+            add_codes(pw[w], a2, a3);
+        }
+        // the same scales as the MMA applies (subnormal 2^-127 for x == 0)
+        const float f0 = x0 ? __int_as_float(x0 << 23) : __int_as_float(0x00400000);
+        const float f1 = x1 ? __int_as_float(x1 << 23) : __int_as_float(0x00400000);
+        l = l * alpha + ((a0 + a1) * f0 + (a2 + a3) * f1);
+        // scale factors: SFA row r at column (32 + quadrant), byte = K-block (32 keys)
+        const uint32_t sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) |
+                             ((uint32_t)x1 << 24);
+        tmem_st1(s_col + 32 + quad, sfa);
+        tmem_st4(s_col + 36, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      } else {
+        float mt = __uint_as_float(s[0]);
+#pragma unroll
+        for (int c = 1; c < 127; c += 2)
+          mt = fmax3(mt, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+        mt = fmaxf(mt, __uint_as_float(s[127])) * lam;  // tile max in log2 units
+        if (!have_ref) {
+          ref = mt;
+          have_ref = true;
+        } else if (mt > ref) {
+          alpha = ex2_approx(ref - mt);
+          ref = mt;
+          rescale = true;
+        }
+        const float nb = -ref;
+        float ls0 = 0.f, ls1 = 0.f;
+        if constexpr (V == kExactFp8) {
+#pragma unroll
+          for (int w = 0; w < 32; ++w) {
+            float pv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, nb));
+            ls0 += pv[0] + pv[2];
+            ls1 += pv[1] + pv[3];
+            const uint32_t lo = f32x2_to_e4m3x2(pv[0], pv[1]);
+            const uint32_t hi = f32x2_to_e4m3x2(pv[2], pv[3]);
+            pw[w] = lo | (hi << 16);
+          }
+          tmem_st1(s_col + 32 + quad, 0x7F7F7F7Fu);
+          tmem_st4(s_col + 36, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+#pragma unroll
+          for (int w = 0; w < 64; ++w) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * w]), lam, nb));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * w + 1]), lam, nb));
+            ls0 += p0;
+            ls1 += p1;
+            __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
+            pw[w] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+        }
+        l = l * alpha + (ls0 + ls1);
+      }
+      // Correct O_t for a raised reference before the next P.V accumulates.
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t o[32];
+          tmem_ld32_wait(o_col + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_col + c, o);
+        }
+      }
+      if constexpr (C::kFp8) {
+        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+      } else {
+        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[t]);
+      ++o_cnt;
+    }
+    // epilogue: out = dv * O / l
+    if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
+    tc_fence_after();
+    const float inv = dvv / l;
+    const bool store = row < p.S;
+    const size_t orow = ((size_t)b * p.S + (size_t)(row < p.S ? row : 0)) * p.Hq + h;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      uint32_t o[32];
+      tmem_ld32_wait(o_col + c, o);
+      if (store) {
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                 __uint_as_float(o[4 * i + 2]) * inv,
+                                 __uint_as_float(o[4 * i + 3]) * inv);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(o[8 * i + 2 * k]) * inv,
+                                                        __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
+              w[k] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(&bars.o_free[t]);
+  }
+}
+
+// --------------------------------------------------------------------------
+// The kernel.
+// --------------------------------------------------------------------------
+template <int V, int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ Maps maps, const KParams p) {
+  using C = Cfg<V, DQK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ Barriers bars;
+  const uint32_t warp = warp_id();
+  if (threadIdx.x == 0) {
+    bars.abort_flag = 0;
+    mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_empty, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.o_done[t], 1);
+      mbar_init(&bars.o_free[t], 128);
+    }
+    mbar_init(&bars.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp < 8) {
+    softmax_loop<V, DQK>(p, bars, tmem, warp / 4);
+  } else if (warp == kProducerWarp) {
+    producer_loop<V, DQK>(p, maps, smem, bars);
+  } else if (warp == kMmaWarp) {
+    mma_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
+    if (lane_id() == 0) {
+      // every MMA this thread issued must be complete before TMEM is released
+      volatile int dummy = 0;
+      tc_commit(&bars.drain);
+      mbar_wait(&bars.drain, 0, &dummy, 50000000ull);
+    }
+    __syncwarp();
+  }
+
+  // Teardown (the producer has already waited for its copies if a role gave up).
+  tc_fence_before();
+  __syncthreads();
+  if (bars.abort_flag && threadIdx.x == 0 && p.status) atomicExch(p.status, 5);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa8

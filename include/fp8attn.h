@@ -1,0 +1,144 @@
+/*
+ * fp8attn.h -- C ABI of the GB300 (sm_103a) causal prefill attention library
+ * (libfp8attn.so).
+ *
+ * The operation is the causal forward ("prefill") attention with equal query
+ * and key lengths that the article "Zyphra ZYFA: FP8 FlashAttention for AMD
+ * MI355X, Up to 1.76x Faster" describes in "TL;DR" (causal forward attention in
+ * FP8 e4m3 and BF16, head dim 128 and the MLA shape 192/128) and whose limits
+ * "Breaking the FP8 Attention Bottleneck on AMD MI355X: How Zyphra ZYFA
+ * Unleashes Performance" states in "Application Boundaries and Engineering
+ * Decisions" (no decode, no paged KV cache, no variable-length batches):
+ *
+ *     out[b, i, h, :] = sum_{j <= i} softmax_j(scale * <q~[b,i,h,:], k~[b,j,g,:]>) v~[b,j,g,:]
+ *
+ * with g = floor(h * Hkv / Hq) (grouped-query head mapping), q~ = dq * q,
+ * k~ = dk * k, v~ = dv * v the dequantized inputs and scale = 1/sqrt(Dqk).
+ *
+ * Three arithmetic paths compute it:
+ *   - attn_fwd_fp8: the Lean-P path.  Each probability is an e4m3 code made by
+ *     one multiply-add and an integer conversion ("Lean P: one multiply-add
+ *     instead of an exponential"); each 64-key block of probabilities carries
+ *     a power-of-two scale that the P.V product removes, and the row is
+ *     divided by the sum of the rounded probabilities ("Per-block scaling and
+ *     a rounded row sum").
+ *   - attn_fwd_fp8_exact: the exact-softmax FP8 ablation (exact exponential,
+ *     probabilities rounded to e4m3, row sum of the unrounded probabilities).
+ *   - attn_fwd_bf16: exact softmax with BF16 inputs and probabilities.
+ *
+ * Layouts (all row-major, contiguous, "BSHD" as in flash_attn_func):
+ *   q   [B, S, Hq,  Dqk]    k [B, S, Hkv, Dqk]    v [B, S, Hkv, Dv]
+ *   out [B, S, Hq,  Dv]     bf16 (or fp32 through attn_fwd_ex)
+ * FP8 inputs are OCP e4m3 bytes; descale_q/k/v point to ONE fp32 each in
+ * DEVICE memory (per-tensor descales), so a call can be captured in a CUDA
+ * graph.  BF16 inputs are bf16 values.
+ *
+ * Supported: causal = 1, (Dqk, Dv) in {(128, 128), (192, 128)} for FP8 and
+ * (128, 128) for BF16, any S >= 1, B >= 1, Hq % Hkv == 0.  Base addresses must
+ * be 16-byte aligned.  The device must be sm_103 (GB300).
+ *
+ * Ownership and threading: the caller owns every buffer.  The library keeps
+ * no per-call allocations and no global mutable state besides a per-device
+ * cache of kernel attributes; calls on different streams may run concurrently.
+ * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ * stream); argument errors are returned synchronously before anything is
+ * launched.
+ */
+#ifndef FP8ATTN_H
+#define FP8ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8ATTN_API_VERSION 1
+
+/* Return codes of every entry point. */
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hq % Hkv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented: causal = 0, other head dims */
+  ATTN_ERR_ARCH = 3,        /* current device is not sm_103 */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map) */
+  ATTN_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (see dev_status) */
+} attn_status;
+
+/* Arithmetic path selector for attn_fwd_ex. */
+typedef enum {
+  ATTN_VARIANT_LEANP = 0,     /* FP8 Lean-P (attn_fwd_fp8) */
+  ATTN_VARIANT_EXACT_FP8 = 1, /* FP8 exact-softmax ablation (attn_fwd_fp8_exact) */
+  ATTN_VARIANT_BF16 = 2       /* BF16 exact softmax (attn_fwd_bf16) */
+} attn_variant;
+
+/* Output element type for attn_fwd_ex. */
+typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
+
+/* attn_fwd_ex flags. */
+#define ATTN_FLAG_NONE 0
+/* Test hook: the load warp issues no copies, so every consumer's bounded wait
+ * expires.  The kernel then sets *dev_status to ATTN_ERR_TIMEOUT and returns
+ * with its tensor memory released.  Requires dev_status != NULL and uses a
+ * short (about 0.2 s) wait limit. */
+#define ATTN_FLAG_TEST_STALL_LOADS 1
+
+/*
+ * FP8 Lean-P causal prefill attention ("Lean P: one multiply-add instead of an
+ * exponential", "Per-block scaling and a rounded row sum").
+ *   q, k, v      device pointers to e4m3 bytes in the layouts above
+ *   descale_*    device pointers to one fp32 each
+ *   out          device pointer, bf16 [B, S, Hq, Dv]
+ *   causal       must be 1
+ *   stream       cudaStream_t or NULL
+ * Returns an attn_status.  A device-side wait expiry cannot be reported here
+ * (nothing is read back); use attn_fwd_ex with dev_status to observe it.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* descale_q,
+                 const float* descale_k, const float* descale_v, void* out, int B, int Hq,
+                 int Hkv, int S, int Dqk, int Dv, int causal, void* stream);
+
+/* FP8 exact-softmax ablation: p = 2^(log2(e) * (z - m)) from the hardware
+ * exponential with a running max m per 128-key tile, P rounded to e4m3
+ * (nearest even), row sum over the unrounded p (the "hardware exponential"
+ * approach in the comparison table of "Zyphra ZYFA: FP8 FlashAttention for AMD
+ * MI355X").  Arguments as attn_fwd_fp8. */
+int attn_fwd_fp8_exact(const void* q, const void* k, const void* v, const float* descale_q,
+                       const float* descale_k, const float* descale_v, void* out, int B,
+                       int Hq, int Hkv, int S, int Dqk, int Dv, int causal, void* stream);
+
+/* BF16 exact-softmax causal prefill attention ("TL;DR": BF16 kernels beside
+ * the FP8 ones).  q, k, v, out are bf16 device pointers; Dqk = Dv = 128. */
+int attn_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                  int S, int Dqk, int Dv, int causal, void* stream);
+
+/*
+ * Extended entry point used by the tests and the benchmark.
+ *   variant        attn_variant
+ *   descale_*      device fp32 pointers (ignored for ATTN_VARIANT_BF16)
+ *   out_dtype      attn_out_dtype; ATTN_OUT_F32 writes fp32 [B, S, Hq, Dv]
+ *   softmax_scale  <= 0 selects 1/sqrt(Dqk)
+ *   flags          ATTN_FLAG_* bits
+ *   dev_status     NULL, or a device int the CALLER zeroes before the call;
+ *                  the kernel stores ATTN_ERR_TIMEOUT there if a bounded wait
+ *                  expired (the output is then undefined).  Read it after the
+ *                  stream has synchronised.
+ */
+int attn_fwd_ex(int variant, const void* q, const void* k, const void* v, const float* descale_q,
+                const float* descale_k, const float* descale_v, void* out, int out_dtype, int B,
+                int Hq, int Hkv, int S, int Dqk, int Dv, int causal, float softmax_scale,
+                int flags, int* dev_status, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/* Number of kernel launches one call makes (1 for every supported shape;
+ * 0 when S == 0 or B == 0 is rejected).  Lets callers count launches. */
+int attn_launches_per_call(void);
+
+/* Library ABI version (FP8ATTN_API_VERSION of the build). */
+int attn_api_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8ATTN_H */

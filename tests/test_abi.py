@@ -1,0 +1,80 @@
+"""CPU checks of the C-ABI boundary: the library builds for sm_103a, loads,
+exports every function include/fp8attn.h declares, and rejects bad arguments
+before touching any device (so these run without a GPU)."""
+import ctypes
+
+import pytest
+
+import fp8_causal_prefill_flash_gb300 as fa
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa.build()
+    return fa.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = fa.declared_functions()
+    for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
+              "attn_status_string", "attn_launches_per_call", "attn_api_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in fa.declared_functions():
+        assert hasattr(lib, n), n
+    assert lib.attn_api_version() == 1
+    assert lib.attn_launches_per_call() == 1
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert fa.status_string(st)
+    assert fa.status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+MIS = ctypes.c_void_p(0x10001)    # misaligned
+
+
+def call_ex(lib, variant=0, q=P, k=P, v=P, dq=P, dk=P, dv=P, out=P, out_dtype=0, B=1, Hq=2,
+            Hkv=2, S=128, Dqk=128, Dv=128, causal=1, scale=0.0, flags=0, status=None):
+    return lib.attn_fwd_ex(variant, q, k, v, dq, dk, dv, out, out_dtype, B, Hq, Hkv, S, Dqk, Dv,
+                           causal, scale, flags, status, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=None), fa.ATTN_ERR_INVALID_ARG),
+    (dict(out=None), fa.ATTN_ERR_INVALID_ARG),
+    (dict(dq=None), fa.ATTN_ERR_INVALID_ARG),
+    (dict(k=MIS), fa.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), fa.ATTN_ERR_INVALID_ARG),
+    (dict(S=0), fa.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), fa.ATTN_ERR_INVALID_ARG),
+    (dict(variant=7), fa.ATTN_ERR_INVALID_ARG),
+    (dict(out_dtype=3), fa.ATTN_ERR_INVALID_ARG),
+    (dict(flags=1), fa.ATTN_ERR_INVALID_ARG),          # stall test hook needs a status word
+    (dict(scale=float("nan")), fa.ATTN_ERR_INVALID_ARG),
+    (dict(causal=0), fa.ATTN_ERR_UNSUPPORTED),
+    (dict(Dqk=64), fa.ATTN_ERR_UNSUPPORTED),
+    (dict(Dv=64), fa.ATTN_ERR_UNSUPPORTED),
+    (dict(variant=2, Dqk=192), fa.ATTN_ERR_UNSUPPORTED),
+])
+def test_bad_arguments_are_rejected_before_launch(lib, kw, want):
+    assert call_ex(lib, **kw) == want
+
+
+def test_bf16_needs_no_descales(lib):
+    # descales may be NULL on the BF16 path; with causal = 0 the call stops at
+    # the (host-side) support check, before any device work
+    assert call_ex(lib, variant=2, dq=None, dk=None, dv=None, causal=0) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_product_entry_points_check_arguments(lib):
+    assert lib.attn_fwd_fp8(None, P, P, P, P, P, P, 1, 2, 2, 128, 128, 128, 1, None) == \
+        fa.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_fp8_exact(P, P, P, P, P, P, P, 1, 2, 2, 128, 128, 128, 0, None) == \
+        fa.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_bf16(P, P, P, P, 1, 2, 2, 128, 192, 128, 1, None) == \
+        fa.ATTN_ERR_UNSUPPORTED

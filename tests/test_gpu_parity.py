@@ -1,0 +1,206 @@
+"""GPU parity: the sm_103a kernels against the CPU oracle, through the C ABI.
+
+Small and ragged shapes are compared on every row; the invariants of the
+method (rounded row sum, causality, head mapping, determinism) are checked
+bitwise where they are exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_causal_prefill_flash_gb300 as fa
+import oracle
+from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+from gpu_helpers import (BF16_RMS_TOL, EMUL_TOL, FP8_RMS_TOL, check_rows, dev_bf16, dev_fp8,
+                         rel_rms, run_bf16, run_fp8, vmax_fp8)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.build()
+    fa.load_library()
+
+
+def _leanp_parity(case, scale=None):
+    gpu = run_fp8(fa.ATTN_VARIANT_LEANP, case, scale=scale or 0.0)
+    emul, amb = oracle.emul_leanp(case.q, case.k, case.v, case.dq, case.dk, case.dv, scale=scale)
+    check_rows(gpu, emul, amb, vmax_fp8(case))
+    return gpu
+
+
+def test_leanp_h2_s256_d128():
+    case = wl.make_case("fp8_h2_s256_d128")
+    gpu = _leanp_parity(case)
+    ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    assert rel_rms(gpu, ref) <= FP8_RMS_TOL
+    # the bf16-output product entry point agrees with the fp32-output one
+    q, k, v, d = dev_fp8(case)
+    out = fa.attn_fwd_fp8(q, k, v, *d)
+    torch.cuda.synchronize()
+    assert np.max(np.abs(out.float().cpu().numpy() - gpu)) <= 2.0 ** -8 * np.max(np.abs(gpu)) + 1e-6
+
+
+def test_exact_fp8_h2_s256_d128():
+    case = wl.make_case("fp8_h2_s256_d128")
+    gpu = run_fp8(fa.ATTN_VARIANT_EXACT_FP8, case)
+    emul, amb = oracle.emul_exact_fp8(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    check_rows(gpu, emul, amb, vmax_fp8(case))
+    ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    assert rel_rms(gpu, ref) <= FP8_RMS_TOL
+
+
+def test_bf16_h2_s256_d128():
+    case = wl.bf16_gaussian_case(1, 2, 2, 256, 128, 128)
+    gpu = run_bf16(case)
+    ref = oracle.ref_fp64_bf16(case.q, case.k, case.v)
+    assert rel_rms(gpu, ref) <= BF16_RMS_TOL
+    emul = oracle.emul_bf16(case.q, case.k, case.v)
+    vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
+    assert np.max(np.abs(gpu - emul)) <= EMUL_TOL * vmax
+
+
+@pytest.mark.parametrize("S", [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 600])
+def test_leanp_ragged_lengths(S):
+    case = wl.fp8_gaussian_case(1, 2, 1, S, 128, 128, seeds=(100 + S, 200 + S, 300 + S))
+    _leanp_parity(case)
+
+
+@pytest.mark.parametrize("S", [1, 65, 200, 513])
+def test_exact_fp8_ragged_lengths(S):
+    case = wl.fp8_gaussian_case(1, 2, 1, S, 128, 128, seeds=(400 + S, 500 + S, 600 + S))
+    gpu = run_fp8(fa.ATTN_VARIANT_EXACT_FP8, case)
+    emul, amb = oracle.emul_exact_fp8(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    check_rows(gpu, emul, amb, vmax_fp8(case))
+
+
+@pytest.mark.parametrize("S", [1, 100, 300])
+def test_bf16_ragged_lengths(S):
+    case = wl.bf16_gaussian_case(1, 2, 1, S, 128, 128, seeds=(S, S + 1, S + 2))
+    gpu = run_bf16(case)
+    emul = oracle.emul_bf16(case.q, case.k, case.v)
+    vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
+    assert np.max(np.abs(gpu - emul)) <= EMUL_TOL * vmax
+
+
+def test_leanp_gqa_and_batch():
+    case = wl.fp8_gaussian_case(2, 8, 2, 300, 128, 128, seeds=(21, 22, 23), outlier_seed=24,
+                                outliers_qk=1, factor=8.0)
+    _leanp_parity(case)
+
+
+def test_leanp_mla_shape():
+    case = wl.fp8_gaussian_case(1, 2, 2, 333, 192, 128, seeds=(31, 32, 33), outlier_seed=34,
+                                outliers_qk=4, factor=20.0, outliers_v=False)
+    gpu = _leanp_parity(case)
+    ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    assert rel_rms(gpu, ref) <= FP8_RMS_TOL
+
+
+def test_exact_fp8_mla_shape():
+    case = wl.fp8_gaussian_case(1, 2, 2, 260, 192, 128, seeds=(35, 36, 37))
+    gpu = run_fp8(fa.ATTN_VARIANT_EXACT_FP8, case)
+    emul, amb = oracle.emul_exact_fp8(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    check_rows(gpu, emul, amb, vmax_fp8(case))
+
+
+def test_explicit_softmax_scale():
+    case = wl.fp8_gaussian_case(1, 1, 1, 200, 128, 128, seeds=(41, 42, 43))
+    _leanp_parity(case, scale=0.21)
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_v_ones_gives_exactly_one():
+    """Rounded row sum: with V = 1 every Lean-P output is exactly 1.0 in bf16."""
+    case = wl.fp8_gaussian_case(1, 4, 2, 700, 128, 128, seeds=(51, 52, 53))
+    q, k, v, d = dev_fp8(case)
+    v = torch.full_like(v, 0x38)
+    d[2] = torch.ones(1, dtype=torch.float32, device="cuda")
+    out = fa.attn_fwd_fp8(q, k, v, *d)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 1.0)
+
+
+def test_q_zero_gives_prefix_mean():
+    case = wl.fp8_gaussian_case(1, 2, 2, 300, 128, 128, seeds=(54, 55, 56))
+    q, k, v, d = dev_fp8(case)
+    q.zero_()
+    out = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d).cpu().numpy()
+    vf = oracle.e4m3_decode(case.v) * case.dv
+    want = np.cumsum(vf, axis=1) / np.arange(1, 301)[None, :, None, None]
+    assert np.max(np.abs(out - want)) <= 1e-5 * np.max(np.abs(vf))
+
+
+def test_future_keys_do_not_change_earlier_rows():
+    case = wl.fp8_gaussian_case(1, 2, 1, 512, 128, 128, seeds=(57, 58, 59))
+    q, k, v, d = dev_fp8(case)
+    a = fa.attn_fwd_fp8(q, k, v, *d).clone()
+    i0 = 300
+    k2, v2 = k.clone(), v.clone()
+    k2[:, i0 + 1:] = torch.randint(0, 126, k2[:, i0 + 1:].shape, dtype=torch.uint8, device="cuda")
+    v2[:, i0 + 1:] = torch.randint(0, 126, v2[:, i0 + 1:].shape, dtype=torch.uint8, device="cuda")
+    b = fa.attn_fwd_fp8(q, k2, v2, *d)
+    torch.cuda.synchronize()
+    assert torch.equal(a[:, :i0 + 1], b[:, :i0 + 1])
+
+
+def test_gqa_equals_repeated_heads():
+    case = wl.fp8_gaussian_case(1, 6, 2, 260, 128, 128, seeds=(61, 62, 63))
+    q, k, v, d = dev_fp8(case)
+    a = fa.attn_fwd_fp8(q, k, v, *d)
+    b = fa.attn_fwd_fp8(q, k.repeat_interleave(3, dim=2).contiguous(),
+                        v.repeat_interleave(3, dim=2).contiguous(), *d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_repeated_launches_are_bitwise_identical():
+    case = wl.fp8_gaussian_case(1, 4, 4, 1024, 128, 128, seeds=(64, 65, 66))
+    q, k, v, d = dev_fp8(case)
+    first = fa.attn_fwd_fp8(q, k, v, *d).clone()
+    for _ in range(50):
+        again = fa.attn_fwd_fp8(q, k, v, *d)
+        assert torch.equal(first, again)
+
+
+# ------------------------------------------------------------------ failure paths
+
+def test_stalled_loads_report_timeout_and_context_survives():
+    """Test hook: no copies are issued, every bounded wait expires, the kernel
+    reports ATTN_ERR_TIMEOUT in the status word and the context stays usable."""
+    case = wl.fp8_gaussian_case(1, 2, 2, 256, 128, 128, seeds=(1, 2, 3))
+    q, k, v, d = dev_fp8(case)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d, flags=fa.ATTN_FLAG_TEST_STALL_LOADS,
+                   dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.ATTN_ERR_TIMEOUT
+    # the next normal call works and agrees with the oracle
+    status.zero_()
+    gpu = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    emul, amb = oracle.emul_leanp(case.q, case.k, case.v, case.dq, case.dk, case.dv)
+    check_rows(gpu.cpu().numpy().astype(np.float64), emul, amb, vmax_fp8(case))
+
+
+def test_argument_errors_are_reported():
+    case = wl.fp8_gaussian_case(1, 2, 2, 64, 128, 128)
+    q, k, v, d = dev_fp8(case)
+    _, st = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d, causal=False, raise_on_error=False)
+    assert st == fa.ATTN_ERR_UNSUPPORTED
+    q3 = torch.zeros((1, 64, 3, 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_fwd_fp8(q3, k, v, *d)
+    assert e.value.status == fa.ATTN_ERR_INVALID_ARG
+    q64 = torch.zeros((1, 64, 2, 64), dtype=torch.uint8, device="cuda")
+    k64 = torch.zeros((1, 64, 2, 64), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.AttnError) as e:
+        fa.attn_fwd_fp8(q64, k64, v, *d)
+    assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
