@@ -1,0 +1,372 @@
+#!/usr/bin/env python3
+"""Benchmark of FP8 Lean-P causal prefill attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of the whole hot path -- ``attn_fwd_fp8`` (one kernel
+launch) -- on the headline workload: FP8 e4m3, B=1, Hq=Hkv=32, S=32768,
+Dqk=Dv=128, Gaussian inputs quantised per tensor.  Q, K and V (3 x 134 MB)
+exceed the 129 MB L2, so no flush is needed between steps.
+
+Rank 0 prints one JSON line.  ``value`` is TFLOP/s over all ranks with the
+algorithmic causal FLOP count 2*B*Hq*(Dqk+Dv)*S*(S+1)/2; the count of the
+formula 2*B*Hq*S^2*(Dqk+Dv) (twice the causal work) is reported beside it.
+Under torchrun every rank runs its own copy of the workload (independent
+problems, no collective on the data path: weak scaling).
+
+``--impl reference`` times the CPU oracle (the Lean-P emulation) on the host
+cores instead, on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "fp8_h32_s32k_d128"
+METRIC = "causal prefill attn TFLOP/s (FP8 hd128 S=32K) and % of GB300 dense FP8 peak"
+FP8_OVER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor-core ratio (4.5 : 2.25 PFLOP/s)
+
+
+def causal_flops(B, Hq, S, Dqk, Dv):
+    return 2.0 * B * Hq * (Dqk + Dv) * S * (S + 1) / 2.0
+
+
+def square_flops(B, Hq, S, Dqk, Dv):
+    return 2.0 * B * Hq * S * S * (Dqk + Dv)
+
+
+def rows_flops(rows, Dqk, Dv):
+    return float(sum(2.0 * (Dqk + Dv) * (int(i) + 1) for _, _, i in rows))
+
+
+def max_over_ranks(ms, device=None):
+    """Largest per-rank step time (the job is as slow as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, world, ms_max):
+    """Whole-job throughput: every rank processes its own copy of the workload."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_burst": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) taken while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid=None):
+        self.proc = None
+        self.lines = []
+        self.gpu = gpu_uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu:
+            cmd += ["-i", self.gpu]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[5:9]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- oracle arm
+def sample_rows(S, Hq, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([np.zeros(n, np.int64), rng.integers(0, Hq, n), rng.integers(0, S, n)], 1)
+
+
+def oracle_leg(case, rows):
+    """Time the CPU oracle (Lean-P emulation, as it stands) on `rows`."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    out, _ = oracle.emul_leanp(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
+    dt = time.perf_counter() - t0
+    return out, dt
+
+
+def cores_used():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+    case = wl.make_case(WORKLOAD)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    # bounded sample: about args.ref_row_budget rows over the whole run
+    n_rows = max(4, args.ref_row_budget // (args.warmup + args.steps))
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = sample_rows(S, Hq, n_rows, 1000 + step)
+        _, dt = oracle_leg(case, rows)
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(rows_flops(rows, Dqk, Dv))
+    tflops = sum(flops) / sum(times) / 1e12
+    sample = (f"{n_rows} random (head, row) pairs of the {WORKLOAD} workload per step, "
+              f"oracle_emul_leanp (C, fp64, OpenMP)")
+    line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "Dqk": Dqk,
+                       "Dv": Dv, "sample_rows_per_step": n_rows},
+            "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import fp8_causal_prefill_flash_gb300 as fa
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa.build()
+    fa.load_library()
+
+    workload = args.workload
+    case = wl.make_case(workload, S=args.S)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    F = causal_flops(B, Hq, S, Dqk, Dv)
+    Fsq = square_flops(B, Hq, S, Dqk, Dv)
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    hq, hk, hv = pin(case.q), pin(case.k), pin(case.v)
+    q, k, v = (t.to(dev) for t in (hq, hk, hv))
+    d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+    out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def step():
+        fa.attn_fwd_fp8(q, k, v, *d, out=out)
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1) / n, dev)
+
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ms = timed(step, args.steps, 0)
+    clk = clocks.stop()
+    if args.leanp_only:
+        if rank == 0:
+            print(json.dumps({"workload": workload, "S": S, "ms_per_step": ms,
+                              "tflops": F / (ms * 1e-3) / 1e12}), flush=True)
+        return 0
+
+    # exact-softmax FP8 ablation, same workload
+    def step_abl():
+        fa.attn_fwd_fp8_exact(q, k, v, *d, out=out)
+    ms_abl = timed(step_abl, max(3, args.steps // 4), 3)
+
+    # end to end through the public API with host buffers: H2D of q, k, v from
+    # pinned memory, the call, D2H of the output into pinned memory
+    hout = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16).pin_memory()
+
+    def step_e2e():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        fa.attn_fwd_fp8(q, k, v, *d, out=out)
+        hout.copy_(out, non_blocking=True)
+    ms_e2e = timed(step_e2e, max(3, args.steps // 10), 2)
+    h2d = hq.numel() + hk.numel() + hv.numel()
+    d2h = hout.numel() * 2
+
+    peaks = load_peaks()
+    peak_fp8 = peaks["bf16_burst"] * FP8_OVER_BF16
+    per_gpu = F / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": job_tflops(F, world, ms), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": workload, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "Dqk": Dqk,
+                       "Dv": Dv, "inputs": "N(0,1) per-tensor e4m3, seeds 30/31/32",
+                       "l2": "inputs (403 MB) larger than L2 (129 MB); no flush",
+                       "flop_count": "causal 2*B*Hq*(Dqk+Dv)*S*(S+1)/2 per rank"},
+            "value_square_formula": job_tflops(Fsq, world, ms),
+            "frac_of_fp8_peak": per_gpu / peak_fp8,
+            "ablation_exact_fp8": {"value": job_tflops(F, world, ms_abl), "ms_per_step": ms_abl},
+            "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak_fp8,
+                         "unit": "TFLOP/s", "frac": per_gpu / peak_fp8, "traffic": args.traffic,
+                         "peak_note": (f"{peaks['source']} bf16 burst {peaks['bf16_burst']} "
+                                       f"TFLOP/s x {FP8_OVER_BF16} (nominal FP8:BF16)")},
+            "e2e": {"value": job_tflops(F, world, ms_e2e), "unit": "TFLOP/s",
+                    "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": args.steps,
+            "clocks": clk}
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        # CPU oracle on a bounded sample of the same workload, and the accuracy
+        # of both GPU paths on those rows against fp64 attention
+        import oracle
+        rows = sample_rows(S, Hq, args.cpu_rows, 7)
+        emu, dt = oracle_leg(case, rows)
+        line["cpu_baseline"] = {
+            "value": rows_flops(rows, Dqk, Dv) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": cores_used(), "kind": "oracle",
+            "sample": f"{len(rows)} random (head, row) pairs of {workload}, oracle_emul_leanp, "
+                      f"{dt:.1f} s"}
+        acc_rows = rows[: args.acc_rows]
+        ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=acc_rows)
+        o_lp = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d).cpu().numpy()
+        o_ab = fa.attn_fwd_ex(fa.ATTN_VARIANT_EXACT_FP8, q, k, v, *d).cpu().numpy()
+        pick = lambda o, rr: np.stack([o[b, i, h] for b, h, i in rr]).astype(np.float64)
+        rel = lambda x: float(np.sqrt(np.mean((x - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))
+        e_lp, e_ab = rel(pick(o_lp, acc_rows)), rel(pick(o_ab, acc_rows))
+        line["accuracy_sampled_rows"] = {
+            "rows": len(acc_rows), "leanp_rel_rms_vs_fp64": e_lp,
+            "ablation_rel_rms_vs_fp64": e_ab, "leanp_over_ablation": e_lp / e_ab,
+            "leanp_max_abs_vs_emulation": float(np.max(np.abs(pick(o_lp, rows) - emu)))}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=4096,
+                    help="oracle rows timed for cpu_baseline (about 10-30 s of CPU work)")
+    ap.add_argument("--acc-rows", type=int, default=1024,
+                    help="rows compared with fp64 attention for the accuracy report")
+    ap.add_argument("--ref-row-budget", type=int, default=8192,
+                    help="oracle rows over the whole reference run")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the same kernel")
+    ap.add_argument("--workload", default=WORKLOAD, help="configuration name (profiling)")
+    ap.add_argument("--S", type=int, default=None, help="override the sequence length (profiling)")
+    ap.add_argument("--leanp-only", action="store_true",
+                    help="time only the Lean-P kernel and print a short line (profiling)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"warning: WORLD_SIZE={world} but --gpus={args.gpus}", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
