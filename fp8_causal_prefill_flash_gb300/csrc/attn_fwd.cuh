@@ -3,29 +3,40 @@
 // One persistent CTA per SM.  A work item is (batch b, query head h, query
 // block qb) with two 128-row query tiles (rows 256*qb .. 256*qb+255); the two
 // tiles share every K/V tile that TMA brings in.  Roles (12 warps):
-//   warps 0-3   softmax warpgroup 0 (query tile 0, thread = row)
-//   warps 4-7   softmax warpgroup 1 (query tile 1)
+//   warps 0-3   softmax of query tile 0 (thread = row)
+//   warps 4-7   softmax of query tile 1
 //   warp  8     TMA producer: Q tiles once per item, K/V tiles through a ring
-//   warp  9     MMA issuer (one thread) and tensor-memory owner
-//   warps 10-11 idle (complete the last warpgroup)
-// Tensor memory (512 columns x 128 lanes of 32-bit):
-//   [  0,128) S0 / P0    [128,256) S1 / P1    [256,384) O0    [384,512) O1
-// S_t = Q_t K_j^T lands in its region; the softmax warpgroup reads it, then
-// writes the probabilities P_t (FP8 codes: 32 columns, BF16: 64 columns) and
-// the block-scale factors into the same region, where the P.V MMA reads them.
-// The MMA issue order per key tile j is PV0(j), QK0(j+1), PV1(j), QK1(j+1),
-// so the softmax of one query tile overlaps the tensor-core work of the other
-// ("two-wave ping-pong" in "Zyphra ZYFA: FP8 FlashAttention for AMD MI355X",
-// "How does ZYFA work?", re-expressed with asynchronous tcgen05 MMAs whose
-// completion mbarriers track, instead of instruction ordering).
+//   warp  9     QK issuer: S = Q_t K_j^T for (j, t) = (0,0), (0,1), (1,0), ...
+//   warp  10    PV issuer: O_t += P_t V_j; owns tensor memory
+//   warp  11    idle (completes the last warpgroup)
+//
+// Tensor memory (512 columns x 128 lanes of 32-bit words), FP8 paths:
+//   S [0,128)  shared by both query tiles, handed over S0(j), S1(j), S0(j+1)...
+//   P0 [128,160) SFA0 [160,164)  P1 [176,208) SFA1 [208,212)  SFB [216,221)
+//   O0 [224,368)  O1 [368,512)   (144 columns: value dims + the row-sum column)
+// BF16 path: S [0,128)  P0 [128,192)  P1 [192,256)  O0 [256,384)  O1 [384,512).
+//
+// A QK product is issued as soon as the softmax warpgroup that owned S has
+// copied it into registers, so S for the next tile is computed while the
+// softmax still works on the current one, and the P.V products are issued by
+// their own warp whenever a P_t(j) is ready.  The softmax of each tile thus
+// hides behind a whole period of tensor-core work (both tiles' QK and PV).
+// Two issuing warps matter on this hardware: a thread that issues tcgen05.mma
+// stalls on any later wait until its own MMAs drain, which idles the pipe
+// unless another thread is issuing.  This replaces the "two-wave ping-pong"
+// of the MI355X design ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X",
+// "How does ZYFA work?"): asynchronous tcgen05 MMAs tracked by mbarriers
+// provide the overlap.
 //
 // Probability policies (softmax warpgroups):
 //   kLeanP     one multiply-add per probability rounded toward minus infinity
 //              into the magic range [2^23, 2^24), whose low byte is the e4m3
 //              code ("Lean P: one multiply-add instead of an exponential"); a
 //              power-of-two scale per 64-key block enters the P.V MMA as a
-//              UE8M0 block-scale factor and the row sum adds the rounded
-//              probabilities ("Per-block scaling and a rounded row sum").
+//              UE8M0 block-scale factor, and the P.V product runs against
+//              [V | ones] so that column 128 of O accumulates the sum of the
+//              rounded, scaled probabilities ("Per-block scaling and a rounded
+//              row sum").
 //   kExactFp8  p = 2^(x - m) on the MUFU, rounded to e4m3, unrounded row sum.
 //   kBf16      as kExactFp8 with bf16 operands and probabilities.
 #pragma once
@@ -39,6 +50,20 @@
 
 namespace fa8 {
 
+// Optional role timeline (debug builds with -DFA8_TIMELINE): clock64 stamps of
+// CTA 0's first item, one row of stamps per key tile, written to fa8_timeline.
+#ifdef FA8_TIMELINE
+__device__ unsigned long long fa8_timeline[4][64][8];
+#define FA8_TL(role, j, k)                                                    \
+  do {                                                                        \
+    if (blockIdx.x == 0 && (j) < 64) fa8_timeline[role][j][k] = clock64();    \
+  } while (0)
+#else
+#define FA8_TL(role, j, k) \
+  do {                     \
+  } while (0)
+#endif
+
 enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2 };
 
 constexpr int kBM = 128;  // query rows per tile
@@ -46,7 +71,8 @@ constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kDV = 128;  // value head dim
 constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kQkWarp = 9;
+constexpr int kPvWarp = 10;  // also allocates tensor memory
 
 // Lean-P constants.  T = 7 headroom binades: the largest probability of each
 // 64-key block gets a code in [C-8, C], C = 8*(7+T) = 112 (the code of 2^T).
@@ -73,11 +99,21 @@ struct Cfg {
   static constexpr int kSmemQ = 0;
   static constexpr int kSmemK = 2 * kQkTileBytes;
   static constexpr int kSmemV = kSmemK + kStages * kQkTileBytes;
-  static constexpr int kSmemBytes = kSmemV + kStages * kVTileBytes;
+  // Lean-P: 128 keys x 128 bytes of e4m3 1.0, the second N-atom of the P.V
+  // B operand, so that O's column 128 accumulates the rounded row sum
+  static constexpr int kOnesBytes = V == kLeanP ? 128 * 128 : 0;
+  static constexpr int kSmemOnes = kSmemV + kStages * kVTileBytes;
+  static constexpr int kSmemBytes = kSmemOnes + kOnesBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kQkSteps = kRowBytes / 32;       // one MMA per 32 bytes of K
   static constexpr int kPvSteps = kFp8 ? 4 : 8;         // 128 keys / (32 fp8 or 16 bf16)
   static constexpr int kPCols = kFp8 ? 32 : 64;         // TMEM columns of P per tile
+  static constexpr int kPvN = V == kLeanP ? 144 : 128;  // P.V N (with the ones column)
+  // tensor-memory columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColP0 = 128, kColP1 = kFp8 ? 176 : 192;
+  static constexpr uint32_t kColSfb = 216;  // FP8 only
+  static constexpr uint32_t kColO0 = kFp8 ? 224 : 256, kColO1 = kFp8 ? 368 : 384;
   static_assert(kTailBytes == 0 || kTailBytes == 64, "row bytes must be 128*n or 128*n+64");
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -130,8 +166,12 @@ __device__ __forceinline__ int kv_tiles_for(const KParams& p, int qb, int t) {
 struct __align__(8) Barriers {
   uint64_t q_full, q_empty;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-  uint64_t drain;
+  uint64_t s_full[2];     // S holds S_t(j) (QK commit)
+  uint64_t s_drained[2];  // softmax t has copied S into registers
+  uint64_t p_full[2];     // softmax t has written P_t(j)
+  uint64_t o_done[2];     // PV_t(j) complete (PV commit)
+  uint64_t o_free[2];     // softmax t has read O_t in its epilogue
+  uint64_t drain[2];      // teardown: all MMAs of the QK / PV warp complete
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -207,7 +247,7 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
 }
 
 // --------------------------------------------------------------------------
-// MMA warp: one thread issues every tcgen05.mma.
+// MMA issue.
 // --------------------------------------------------------------------------
 template <int V, int DQK>
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, int t, uint32_t k_off) {
@@ -229,9 +269,9 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, int 
       bdesc = smem_desc(smem_base + k_off + o, 16, 512, 4);
     }
     if constexpr (C::kFp8)
-      mma_f8_ss(tmem + t * 128, a, bdesc, idesc, k > 0);
+      mma_f8_ss(tmem + C::kColS, a, bdesc, idesc, k > 0);
     else
-      mma_f16_ss(tmem + t * 128, a, bdesc, idesc, k > 0);
+      mma_f16_ss(tmem + C::kColS, a, bdesc, idesc, k > 0);
   }
 }
 
@@ -239,16 +279,18 @@ template <int V, int DQK>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int t, uint32_t v_off,
                                          bool accumulate) {
   using C = Cfg<V, DQK>;
-  const uint32_t d = tmem + 256 + t * 128;
-  const uint32_t a = tmem + t * 128;  // P at the start of the S region
+  const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+  const uint32_t a = tmem + (t ? C::kColP1 : C::kColP0);
   if constexpr (C::kFp8) {
-    const uint32_t sfa = tmem + t * 128 + 32;  // + lane quadrant (per the MMA's read pattern)
-    const uint32_t sfb = tmem + t * 128 + 36;
+    // SFA of P_t at a + 32 (+ lane quadrant, the MMA's read pattern), byte =
+    // K-step; SFB (all 1.0) at kColSfb.  Lean-P: B = [V | ones], the ones atom
+    // at LBO after the V stage; N = 128 otherwise.
+    const uint32_t lbo = C::kOnesBytes ? (uint32_t)(C::kSmemOnes - (int)v_off) : 1024u;
 #pragma unroll
     for (int k = 0; k < C::kPvSteps; ++k) {
-      const uint64_t bdesc = smem_desc(smem_base + v_off + 4096 * k, 1024, 1024, kSwizzle128B);
-      mma_mx8_ts(d, a + 8 * k, bdesc, idesc_mx(128, 128, 0, 0, 0, 1, k, k), sfa, sfb,
-                 accumulate || k > 0);
+      const uint64_t bdesc = smem_desc(smem_base + v_off + 4096 * k, lbo, 1024, kSwizzle128B);
+      mma_mx8_ts(d, a + 8 * k, bdesc, idesc_mx(128, C::kPvN, 0, 0, 0, 1, k, k), a + 32,
+                 tmem + C::kColSfb, accumulate || k > 0);
     }
   } else {
     constexpr uint32_t idesc = idesc_f32acc(128, 128, 1, 1, 0, 1);
@@ -261,78 +303,82 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int 
   }
 }
 
+// QK warp: S = Q_t K_j^T in the order S0(0), S1(0), S0(1), S1(1), ... (tile 0
+// skips key tiles past its diagonal).  Each product waits until the previous
+// owner of S has copied it out.
 template <int V, int DQK>
-__device__ void mma_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
+__device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
   using C = Cfg<V, DQK>;
   if (lane_id() != 0) return;
   volatile int* ab = &bars.abort_flag;
   const uint64_t lim = p.wait_limit_ns;
   uint32_t kv_it = 0, q_it = 0;
-  uint32_t p_cnt[2] = {0, 0}, items_t[2] = {0, 0};
+  uint32_t issued[2] = {0, 0};  // S products issued per tile
+  int last = -1;                // tile of the previous S product
   for (int round = 0;; ++round) {
     const int idx = item_at(round, p.n_items);
     if (idx < 0) break;
     int b, h, qb;
     decode_item(p, idx, b, h, qb);
-    const int nkv0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
+    const int nk0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
     if (!mbar_wait(&bars.q_full, q_it & 1, ab, lim)) return;
     ++q_it;
-    tc_fence_after();
-    // prologue: S_t(0) for both tiles
-    {
+    for (int j = 0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
       if (!mbar_wait(&bars.k_full[st], ph, ab, lim)) return;
-      tc_fence_after();
-      const uint32_t k_off = smem_base + C::kSmemK + st * C::kQkTileBytes - smem_base;
       for (int t = 0; t < 2; ++t) {
-        if (0 < (t ? nkv : nkv0)) {
-          issue_qk<V, DQK>(tmem, smem_base, t, k_off);
-          tc_commit(&bars.s_full[t]);
-        }
+        if (j >= (t ? nkv : nk0)) continue;
+        if (last >= 0 &&
+            !mbar_wait(&bars.s_drained[last], (issued[last] - 1) & 1, ab, lim))
+          return;
+        tc_fence_after();
+        issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + st * C::kQkTileBytes);
+        tc_commit(&bars.s_full[t]);
+        ++issued[t];
+        last = t;
       }
       tc_commit(&bars.k_empty[st]);
-      if (nkv == 1) tc_commit(&bars.q_empty);
     }
-    for (int j = 0; j < nkv; ++j) {
-      const uint32_t it = kv_it + j;
-      const uint32_t st = it % C::kStages, ph = (it / C::kStages) & 1;
-      const uint32_t stn = (it + 1) % C::kStages, phn = ((it + 1) / C::kStages) & 1;
-      const bool has_next = j + 1 < nkv;
-      bool next_k_ready = false;
+    tc_commit(&bars.q_empty);
+  }
+}
+
+// PV warp: O_t += P_t V_j as soon as P_t(j) is written.
+template <int V, int DQK>
+__device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
+  using C = Cfg<V, DQK>;
+  if (lane_id() != 0) return;
+  volatile int* ab = &bars.abort_flag;
+  const uint64_t lim = p.wait_limit_ns;
+  uint32_t kv_it = 0, p_cnt[2] = {0, 0}, items = 0;
+  for (int round = 0;; ++round) {
+    const int idx = item_at(round, p.n_items);
+    if (idx < 0) break;
+    int b, h, qb;
+    decode_item(p, idx, b, h, qb);
+    const int nk0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
+    for (int j = 0; j < nkv; ++j, ++kv_it) {
+      const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
+      const bool stamp = round == 0;
       if (!mbar_wait(&bars.v_full[st], ph, ab, lim)) return;
-      tc_fence_after();
-      const uint32_t v_off = C::kSmemV + st * C::kVTileBytes;
       for (int t = 0; t < 2; ++t) {
-        const int nk_t = t ? nkv : nkv0;
-        if (j < nk_t) {
-          if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
-          ++p_cnt[t];
-          if (j == 0) {
-            // the previous item's epilogue must have read O_t
-            if (!mbar_wait(&bars.o_free[t], (items_t[t] & 1) ^ 1, ab, lim)) return;
-            ++items_t[t];
-          }
-          tc_fence_after();
-          issue_pv<V, DQK>(tmem, smem_base, t, v_off, j > 0);
-          tc_commit(&bars.o_done[t]);
+        if (j >= (t ? nkv : nk0)) continue;
+        if (stamp) FA8_TL(2 + t, j, 0);
+        if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
+        ++p_cnt[t];
+        if (j == 0) {
+          // the previous item's epilogue must have read O_t
+          if (!mbar_wait(&bars.o_free[t], (items & 1) ^ 1, ab, lim)) return;
         }
-        if (has_next && j + 1 < nk_t) {
-          if (!next_k_ready) {
-            if (!mbar_wait(&bars.k_full[stn], phn, ab, lim)) return;
-            tc_fence_after();
-            next_k_ready = true;
-          }
-          issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + stn * C::kQkTileBytes);
-          tc_commit(&bars.s_full[t]);
-        }
+        if (stamp) FA8_TL(2 + t, j, 1);
+        tc_fence_after();
+        issue_pv<V, DQK>(tmem, smem_base, t, C::kSmemV + st * C::kVTileBytes, j > 0);
+        tc_commit(&bars.o_done[t]);
+        if (stamp) FA8_TL(2 + t, j, 2);
       }
       tc_commit(&bars.v_empty[st]);
-      if (has_next) {
-        tc_commit(&bars.k_empty[stn]);
-        if (j + 2 == nkv) tc_commit(&bars.q_empty);
-      }
     }
-    kv_it += nkv;
+    ++items;
   }
 }
 
@@ -345,17 +391,21 @@ __device__ __forceinline__ uint32_t pack4_low_bytes(float a, float b, float c, f
   return prmt(ab, cd, 0x5410);
 }
 
-// Sum of the e4m3 values of the four codes in `w`, added to acc0/acc1 in fp32
-// (pairs are added exactly-representable in f16 first).
-__device__ __forceinline__ void add_codes(uint32_t w, float& acc0, float& acc1) {
-  const uint32_t h01 = e4m3x2_to_f16x2(w & 0xFFFFu);
-  const uint32_t h23 = e4m3x2_to_f16x2(w >> 16);
-  uint32_t hs;
-  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(hs) : "r"(h01), "r"(h23));
-  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n add.rn.f32.f16 %0, lo, %0;\n"
-      " add.rn.f32.f16 %1, hi, %1;\n}\n"
-      : "+f"(acc0), "+f"(acc1)
-      : "r"(hs));
+// Largest of the 64 fp32 values s[o .. o+63] (bit patterns): three-input max
+// (ALU pipe) in four independent chains.
+__device__ __forceinline__ float block_max64(const uint32_t (&s)[128], int o) {
+  float m[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = __uint_as_float(s[o + i]);
+#pragma unroll
+  for (int c = 4; c < 60; c += 8) {  // elements 4 .. 59
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m[i] = fmax3(m[i], __uint_as_float(s[o + c + i]), __uint_as_float(s[o + c + 4 + i]));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __uint_as_float(s[o + 60 + i]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
 __device__ __forceinline__ float pow2i(int e) {  // exact 2^e for e in [-126, 127]
@@ -379,8 +429,9 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
   const uint32_t quad = warp_id() & 3;
   const int r = (int)(quad * 32 + lane_id());  // row within the query tile
   const uint32_t lane_base = (quad * 32) << 16;
-  const uint32_t s_col = tmem + lane_base + t * 128;
-  const uint32_t o_col = tmem + lane_base + 256 + t * 128;
+  const uint32_t s_col = tmem + lane_base + C::kColS;
+  const uint32_t p_col = tmem + lane_base + (t ? C::kColP1 : C::kColP0);
+  const uint32_t o_col = tmem + lane_base + (t ? C::kColO1 : C::kColO0);
   float dqk = 1.0f, dvv = 1.0f;
   if constexpr (C::kFp8) {
     dqk = __ldg(p.dq) * __ldg(p.dk);
@@ -398,11 +449,14 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     decode_item(p, idx, b, h, qb);
     const int nk = kv_tiles_for(p, qb, t);
     const int row = qb * 256 + t * 128 + r;
-    float l = 0.0f;
+    float l = 0.0f;    // exact paths: row sum of the unrounded probabilities
     float ref = 0.0f;  // Lean-P: reference binade; exact paths: running max (log2 units)
     bool have_ref = false;
+    const bool stamp = round == 0 && r == 0;
     for (int j = 0; j < nk; ++j) {
+      if (stamp) FA8_TL(t, j, 0);
       if (!warp_wait(&bars.s_full[t], s_cnt & 1, ab, lim)) return;
+      if (stamp) FA8_TL(t, j, 1);
       ++s_cnt;
       tc_fence_after();
       uint32_t s[128];
@@ -414,8 +468,12 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         tmem_ld32x2_wait(s_col, s_col + 32, s0, s1);
         tmem_ld32x2_wait(s_col + 64, s_col + 96, s2, s3);
       }
+      // S is in registers: the QK warp may reuse it for the other tile
+      tc_fence_before();
+      mbar_arrive(&bars.s_drained[t]);
+      if (stamp) FA8_TL(t, j, 2);
       const int key0 = j * kBN;
-      if (key0 + kBN - 1 > row) {  // diagonal (or ragged) tile: mask keys after the row
+      if (key0 + kBN - 1 > row) {  // diagonal tile: mask keys after the row
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (key0 + c > row) s[c] = __float_as_uint(-INFINITY);
@@ -423,16 +481,9 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       bool rescale = false;
       float alpha = 1.0f;
       uint32_t pw[C::kPCols];
+      uint32_t sfa = 0x7F7F7F7Fu;
       if constexpr (V == kLeanP) {
-        // block maxima of the two 64-key blocks
-        float m0 = __uint_as_float(s[0]), m1 = __uint_as_float(s[64]);
-#pragma unroll
-        for (int c = 1; c < 63; c += 2) {
-          m0 = fmax3(m0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-          m1 = fmax3(m1, __uint_as_float(s[64 + c]), __uint_as_float(s[64 + c + 1]));
-        }
-        m0 = fmaxf(m0, __uint_as_float(s[63]));
-        m1 = fmaxf(m1, __uint_as_float(s[127]));
+        const float m0 = block_max64(s, 0), m1 = block_max64(s, 64);
         // block exponents e = ceil(lam*max): the block maximum lands in (2^(T-1), 2^T]
         const float e0 = ceilf(m0 * lam8 * 0.125f), e1 = ceilf(m1 * lam8 * 0.125f);
         const float emax = fmaxf(e0, e1);
@@ -452,7 +503,6 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         // FMA bias per block: magic - 8e + C (exact integers in fp32)
         const float B0 = v0 ? kMagic - 8.0f * e0 + kLeanC : kMagic;
         const float B1 = v1 ? kMagic - 8.0f * e1 + kLeanC : kMagic;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int w = 0; w < 32; ++w) {
           const float Bb = w < 16 ? B0 : B1;
@@ -461,26 +511,11 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           for (int i = 0; i < 4; ++i)
             y[i] = fmaxf(fma_rm(__uint_as_float(s[4 * w + i]), lam8, Bb), kMagic);
           pw[w] = pack4_low_bytes(y[0], y[1], y[2], y[3]);
-          if (w < 16)
-            add_codes(pw[w], a0, a1);
-          else
-            add_codes(pw[w], a2, a3);
         }
-        // the same scales as the MMA applies (subnormal 2^-127 for x == 0)
-        const float f0 = x0 ? __int_as_float(x0 << 23) : __int_as_float(0x00400000);
-        const float f1 = x1 ? __int_as_float(x1 << 23) : __int_as_float(0x00400000);
-        l = l * alpha + ((a0 + a1) * f0 + (a2 + a3) * f1);
-        // scale factors: SFA row r at column (32 + quadrant), byte = K-block (32 keys)
-        const uint32_t sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) |
-                             ((uint32_t)x1 << 24);
-        tmem_st1(s_col + 32 + quad, sfa);
-        tmem_st4(s_col + 36, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        // scale factor bytes: K-steps 0-1 (block 0) and 2-3 (block 1)
+        sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
       } else {
-        float mt = __uint_as_float(s[0]);
-#pragma unroll
-        for (int c = 1; c < 127; c += 2)
-          mt = fmax3(mt, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-        mt = fmaxf(mt, __uint_as_float(s[127])) * lam;  // tile max in log2 units
+        const float mt = fmaxf(block_max64(s, 0), block_max64(s, 64)) * lam;  // log2 units
         if (!have_ref) {
           ref = mt;
           have_ref = true;
@@ -496,15 +531,14 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           for (int w = 0; w < 32; ++w) {
             float pv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, nb));
+            for (int i = 0; i < 4; ++i)
+              pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, nb));
             ls0 += pv[0] + pv[2];
             ls1 += pv[1] + pv[3];
             const uint32_t lo = f32x2_to_e4m3x2(pv[0], pv[1]);
             const uint32_t hi = f32x2_to_e4m3x2(pv[2], pv[3]);
             pw[w] = lo | (hi << 16);
           }
-          tmem_st1(s_col + 32 + quad, 0x7F7F7F7Fu);
-          tmem_st4(s_col + 36, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         } else {
 #pragma unroll
           for (int w = 0; w < 64; ++w) {
@@ -518,9 +552,11 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         }
         l = l * alpha + (ls0 + ls1);
       }
-      // Correct O_t for a raised reference before the next P.V accumulates.
+      if (stamp) FA8_TL(t, j, 3);
+      // P_t(j-1) must have been consumed, and O_t must be final for j-1
+      // before it is corrected for a raised reference.
+      if (j > 0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -530,21 +566,28 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(o_col + c, o);
         }
+        if constexpr (V == kLeanP) {  // the row-sum column
+          const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
+          tmem_st1(o_col + 128, __float_as_uint(lv));
+        }
       }
       if constexpr (C::kFp8) {
-        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        tmem_st1(p_col + 32 + quad, sfa);
       } else {
-        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
-        tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
+        tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        tmem_st32(p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[t]);
+      if (stamp) FA8_TL(t, j, 4);
       ++o_cnt;
     }
     // epilogue: out = dv * O / l
     if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
     tc_fence_after();
+    if constexpr (V == kLeanP) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
     const float inv = dvv / l;
     const bool store = row < p.S;
     const size_t orow = ((size_t)b * p.S + (size_t)(row < p.S ? row : 0)) * p.Hq + h;
@@ -605,14 +648,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.s_drained[t], 128);
       mbar_init(&bars.p_full[t], 128);
       mbar_init(&bars.o_done[t], 1);
       mbar_init(&bars.o_free[t], 128);
+      mbar_init(&bars.drain[t], 1);
     }
-    mbar_init(&bars.drain, 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if constexpr (C::kOnesBytes > 0) {
+    // the ones atom of the P.V B operand: e4m3 1.0 everywhere
+    uint4* ones = reinterpret_cast<uint4*>(smem + C::kSmemOnes);
+    for (int i = threadIdx.x; i < C::kOnesBytes / 16; i += kThreads)
+      ones[i] = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+    fence_proxy_async_smem();
+  }
+  if (warp == kPvWarp) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
@@ -620,18 +671,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  if constexpr (C::kFp8) {
+    // B-operand scale factors of every P.V product: 1.0 (never overwritten)
+    if (warp < 4) {
+      tmem_st4(tmem + ((warp * 32) << 16) + C::kColSfb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+               0x7F7F7F7Fu);
+      tmem_st1(tmem + ((warp * 32) << 16) + C::kColSfb + 4, 0x7F7F7F7Fu);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 
   if (warp < 8) {
     softmax_loop<V, DQK>(p, bars, tmem, warp / 4);
   } else if (warp == kProducerWarp) {
     producer_loop<V, DQK>(p, maps, smem, bars);
-  } else if (warp == kMmaWarp) {
-    mma_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
+  } else if (warp == kQkWarp || warp == kPvWarp) {
+    const int role = warp == kQkWarp ? 0 : 1;
+    if (role == 0)
+      qk_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
+    else
+      pv_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
     if (lane_id() == 0) {
       // every MMA this thread issued must be complete before TMEM is released
       volatile int dummy = 0;
-      tc_commit(&bars.drain);
-      mbar_wait(&bars.drain, 0, &dummy, 50000000ull);
+      tc_commit(&bars.drain[role]);
+      mbar_wait(&bars.drain[role], 0, &dummy, 50000000ull);
     }
     __syncwarp();
   }
@@ -640,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (bars.abort_flag && threadIdx.x == 0 && p.status) atomicExch(p.status, 5);
-  if (warp == kMmaWarp) {
+  if (warp == kPvWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
