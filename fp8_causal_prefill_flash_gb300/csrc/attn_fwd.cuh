@@ -328,12 +328,16 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
       if (!mbar_wait(&bars.k_full[st], ph, ab, lim)) return;
       for (int t = 0; t < 2; ++t) {
         if (j >= (t ? nkv : nk0)) continue;
+        const bool stamp = round == 0;
+        if (stamp) FA8_TL(2 + t, j, 3);
         if (last >= 0 &&
             !mbar_wait(&bars.s_drained[last], (issued[last] - 1) & 1, ab, lim))
           return;
+        if (stamp) FA8_TL(2 + t, j, 4);
         tc_fence_after();
         issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + st * C::kQkTileBytes);
         tc_commit(&bars.s_full[t]);
+        if (stamp) FA8_TL(2 + t, j, 5);
         ++issued[t];
         last = t;
       }
