@@ -389,27 +389,51 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
 // --------------------------------------------------------------------------
 // Softmax warpgroups.
 // --------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t pack4_low_bytes(float a, float b, float c, float d) {
-  const uint32_t ab = prmt(__float_as_uint(a), __float_as_uint(b), 0x0040);
-  const uint32_t cd = prmt(__float_as_uint(c), __float_as_uint(d), 0x0040);
-  return prmt(ab, cd, 0x5410);
+// Four Lean-P codes c_i = clamp(floor(x_i), 0, .) with x_i = s_i*lam8 + C - 8e,
+// one per byte of the result (little-endian, s0 in the low byte).
+// `A` = lam8/128 and `b` = (C - 8e)/128 are exact power-of-two scalings, so
+// t_i = RD(x_i/128) clamped to [0, 1] satisfies floor(128 t_i) = floor(x_i) for
+// x_i >= 0 (floor(x_i)/128 is a float no larger than x_i/128) and 0 below.
+// The floors are then taken two lanes at a time by rounding down into ranges
+// of fixed spacing: 2^31 (spacing 256) turns t into 2^31 + 256 c, adding
+// 1.5*2^23 - 2^31 (exact) rebases it to 1.5*2^23 + 256 c, and a last rounded-down
+// multiply-add of the partner lane (spacing 1) gives 1.5*2^23 + c_lo + 256 c_hi,
+// whose two low bytes are the pair of codes.  Everything but the byte
+// shuffle runs on the FMA pipe.
+struct LeanPConsts {
+  uint64_t k32768, base_hi, rebase, k128;
+};
+__device__ __forceinline__ LeanPConsts leanp_consts() {
+  return {f32x2_pack(32768.0f, 32768.0f), f32x2_pack(2147483648.0f, 2147483648.0f),
+          f32x2_pack(kMagic - 2147483648.0f, kMagic - 2147483648.0f), f32x2_pack(128.0f, 128.0f)};
+}
+__device__ __forceinline__ uint32_t leanp_codes4(float s0, float s1, float s2, float s3, float A,
+                                                 float b, const LeanPConsts& k) {
+  const float t0 = fma_rm_sat(s0, A, b), t1 = fma_rm_sat(s1, A, b);
+  const float t2 = fma_rm_sat(s2, A, b), t3 = fma_rm_sat(s3, A, b);
+  uint64_t z = fma_rm_f32x2(f32x2_pack(t1, t3), k.k32768, k.base_hi);  // 2^31 + 256 c_{1,3}
+  z = add_f32x2(z, k.rebase);                                           // M + 256 c_{1,3}
+  const uint64_t y = fma_rm_f32x2(f32x2_pack(t0, t2), k.k128, z);       // M + c_{0,2} + 256 c_{1,3}
+  uint32_t y01, y23;
+  f32x2_unpack(y, y01, y23);
+  return prmt(y01, y23, 0x5410);
 }
 
-// Largest of the 64 fp32 values s[o .. o+63] (bit patterns): three-input max
-// (ALU pipe) in four independent chains.
+// Largest of the 64 fp32 values s[o .. o+63] (bit patterns): 32 three-input
+// maxima (ALU pipe), four independent chains of 15 elements, then the last
+// four elements folded into the combination.
 __device__ __forceinline__ float block_max64(const uint32_t (&s)[128], int o) {
+  auto f = [&](int i) { return __uint_as_float(s[o + i]); };
   float m[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = __uint_as_float(s[o + i]);
+  for (int i = 0; i < 4; ++i) m[i] = fmax3(f(i), f(4 + i), f(8 + i));  // elements 0 .. 11
 #pragma unroll
-  for (int c = 4; c < 60; c += 8) {  // elements 4 .. 59
+  for (int c = 12; c < 60; c += 8) {  // elements 12 .. 59
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      m[i] = fmax3(m[i], __uint_as_float(s[o + c + i]), __uint_as_float(s[o + c + 4 + i]));
+    for (int i = 0; i < 4; ++i) m[i] = fmax3(m[i], f(c + i), f(c + 4 + i));
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], __uint_as_float(s[o + 60 + i]));
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  const float a = fmax3(m[0], m[1], f(60)), bb = fmax3(m[2], m[3], f(61));
+  return fmax3(a, bb, fmaxf(f(62), f(63)));
 }
 
 __device__ __forceinline__ float pow2i(int e) {  // exact 2^e for e in [-126, 127]
@@ -444,6 +468,8 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
   const float log2e = 1.4426950408889634f;
   const float lam = log2e * p.scale * dqk;  // log2 units per unit of s
   const float lam8 = 8.0f * lam;            // Lean-P code units per unit of s
+  const float lamc = lam8 * (1.0f / 128.0f);
+  const LeanPConsts kc = leanp_consts();
   uint32_t s_cnt = 0, o_cnt = 0;
 
   for (int round = 0;; ++round) {
@@ -504,18 +530,15 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         const bool v0 = e0 > -INFINITY, v1 = e1 > -INFINITY;
         const int x0 = v0 ? max(min((int)(e0 - ref) - kLeanT + 127, 254), 0) : 0;
         const int x1 = v1 ? max(min((int)(e1 - ref) - kLeanT + 127, 254), 0) : 0;
-        // FMA bias per block: magic - 8e + C (exact integers in fp32)
-        const float B0 = v0 ? kMagic - 8.0f * e0 + kLeanC : kMagic;
-        const float B1 = v1 ? kMagic - 8.0f * e1 + kLeanC : kMagic;
+        // bias per block: (C - 8e)/128, exact; a fully masked block has only
+        // -inf scores, which give code 0 whatever the bias
+        const float b0 = v0 ? (kLeanC - 8.0f * e0) * (1.0f / 128.0f) : 0.0f;
+        const float b1 = v1 ? (kLeanC - 8.0f * e1) * (1.0f / 128.0f) : 0.0f;
 #pragma unroll
-        for (int w = 0; w < 32; ++w) {
-          const float Bb = w < 16 ? B0 : B1;
-          float y[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            y[i] = fmaxf(fma_rm(__uint_as_float(s[4 * w + i]), lam8, Bb), kMagic);
-          pw[w] = pack4_low_bytes(y[0], y[1], y[2], y[3]);
-        }
+        for (int w = 0; w < 32; ++w)
+          pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
+                               __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
+                               lamc, w < 16 ? b0 : b1, kc);
         // scale factor bytes: K-steps 0-1 (block 0) and 2-3 (block 1)
         sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
       } else {

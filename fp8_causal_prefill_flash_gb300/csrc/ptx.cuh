@@ -316,11 +316,32 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 }
 
 // ------------------------------------------------------------ scalar helpers
-// fp32 fused multiply-add rounded toward minus infinity.
-__device__ __forceinline__ float fma_rm(float a, float b, float c) {
+// fp32 RD(a*b + c), then clamped to [0, 1] (NaN and -inf give +0).
+__device__ __forceinline__ float fma_rm_sat(float a, float b, float c) {
   float d;
-  asm("fma.rm.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  asm("fma.rm.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+// Two floats in one 64-bit register pair (lane 0 = lo), for the packed
+// f32x2 instructions of sm_100+.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+// Packed RD(a*b + c) on both lanes: one issue slot for two results.
+__device__ __forceinline__ uint64_t fma_rm_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, uint32_t& lo, uint32_t& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
