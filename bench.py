@@ -66,6 +66,33 @@ def job_tflops(flops_per_rank, world, ms_max):
     return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
+# DRAM traffic of one Lean-P launch on the headline workload, read from an ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
+# summary and the command).  It belongs to the kernel sources it was taken
+# with: for any other sources the bench reports null.
+PROFILED_TRAFFIC = {"bytes": 3990294016,
+                    "sources_sha256": "8bc1b03cac4c06c8634160d07b6c604a6111abdfc1b28b6e0629e3f50bb15b07"}
+KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
+                  "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
+                  "fp8_causal_prefill_flash_gb300/csrc/api.cu")
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    if PROFILED_TRAFFIC["bytes"] is None:
+        return None
+    return PROFILED_TRAFFIC["bytes"] if kernel_sources_sha256() == PROFILED_TRAFFIC["sources_sha256"] \
+        else None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -291,7 +318,8 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_fp8_peak": per_gpu / peak_fp8,
             "ablation_exact_fp8": {"value": job_tflops(F, world, ms_abl), "ms_per_step": ms_abl},
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak_fp8,
-                         "unit": "TFLOP/s", "frac": per_gpu / peak_fp8, "traffic": args.traffic,
+                         "unit": "TFLOP/s", "frac": per_gpu / peak_fp8,
+                         "traffic": args.traffic if args.traffic is not None else profiled_traffic(),
                          "peak_note": (f"{peaks['source']} bf16 burst {peaks['bf16_burst']} "
                                        f"TFLOP/s x {FP8_OVER_BF16} (nominal FP8:BF16)")},
             "e2e": {"value": job_tflops(F, world, ms_e2e), "unit": "TFLOP/s",
@@ -327,13 +355,67 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def run_sweep(args):
+    """One JSON line per configuration of the workload table (measurement
+    notes, not the bench line): each path's time, causal TFLOP/s and fraction
+    of the matching measured peak; for the short case also HBM GB/s."""
+    import torch
+
+    import fp8_causal_prefill_flash_gb300 as fa
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+    fa.build()
+    fa.load_library()
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    for name, cfg in wl.CONFIGS.items():
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        F = causal_flops(B, Hq, S, Dqk, Dv)
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+        if cfg["kind"] == "fp8":
+            q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+            d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+            paths = {"leanp": lambda: fa.attn_fwd_fp8(q, k, v, *d, out=out),
+                     "exact_fp8_ablation": lambda: fa.attn_fwd_fp8_exact(q, k, v, *d, out=out)}
+            peak = peaks["bf16_burst"] * FP8_OVER_BF16
+            in_bytes = (case.q.nbytes + case.k.nbytes + case.v.nbytes)
+        else:
+            q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                       for a in (case.q, case.k, case.v))
+            paths = {"bf16": lambda: fa.attn_fwd_bf16(q, k, v, out=out)}
+            peak = peaks["bf16_burst"]
+            in_bytes = 2 * (case.q.size + case.k.size + case.v.size)
+        io_bytes = in_bytes + out.numel() * 2
+        for path, fn in paths.items():
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            n = args.steps
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            tf = F / (ms * 1e-3) / 1e12
+            print(json.dumps({"workload": name, "path": path, "ms": ms, "tflops_causal": tf,
+                              "tflops_square_formula": 2 * tf, "peak": peak,
+                              "frac_of_peak": tf / peak, "hbm_gbs": io_bytes / (ms * 1e-3) / 1e9,
+                              "peak_source": peaks["source"], "iterations": n}), flush=True)
+        del q, k, v, out
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=4096,
+    ap.add_argument("--cpu-rows", type=int, default=8192,
                     help="oracle rows timed for cpu_baseline (about 10-30 s of CPU work)")
     ap.add_argument("--acc-rows", type=int, default=1024,
                     help="rows compared with fp64 attention for the accuracy report")
@@ -346,6 +428,8 @@ def main():
     ap.add_argument("--S", type=int, default=None, help="override the sequence length (profiling)")
     ap.add_argument("--leanp-only", action="store_true",
                     help="time only the Lean-P kernel and print a short line (profiling)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every path on every configuration, one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -356,6 +440,8 @@ def main():
         print(f"warning: WORLD_SIZE={world} but --gpus={args.gpus}", file=sys.stderr)
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        return run_sweep(args)
     if world > 1:
         import torch
         import torch.distributed as dist
