@@ -373,7 +373,7 @@ def run_sweep(args):
         B, Hq, Hkv, S, Dqk, Dv = case.shape
         F = causal_flops(B, Hq, S, Dqk, Dv)
         out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
-        if cfg["kind"] == "fp8":
+        if cfg["kind"].startswith("fp8"):
             q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
             d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
             paths = {"leanp": lambda: fa.attn_fwd_fp8(q, k, v, *d, out=out),

@@ -106,6 +106,31 @@ def fp8_gaussian_case(B, Hq, Hkv, S, Dqk, Dv, seeds=(0, 1, 2), outlier_seed: Opt
     return Fp8Case(qc, kc, vc, dq, dk, dv)
 
 
+def fp8_sink_case(B, Hq, Hkv, S, Dqk, Dv, seeds=(50, 51, 52), sink_logits=(15.0, 25.0),
+                  v_mean=1.0, sink_channel=0, scale=None) -> Fp8Case:
+    """Gaussian Q, K, V plus an attention sink: key 0 of every kv head gets a
+    large value in one channel, and every query row a per-row weight in that
+    channel, so that row i's logit for key 0 exceeds the others by a value
+    drawn uniformly from ``sink_logits`` (natural-log units, softmax scale
+    ``scale``, default 1/sqrt(Dqk)).  The row maxima thus differ row by row
+    and dwarf the rest of the row; V has mean ``v_mean``."""
+    scale = 1.0 / np.sqrt(Dqk) if scale is None else scale
+    q = gaussian((B, S, Hq, Dqk), seeds[0])
+    k = gaussian((B, S, Hkv, Dqk), seeds[1])
+    v = gaussian((B, S, Hkv, Dv), seeds[2]) + np.float32(v_mean)
+    rng = np.random.default_rng(seeds[0] + 1000)
+    amp = np.float32(32.0)
+    k[:, 0, :, sink_channel] = amp
+    target = rng.uniform(sink_logits[0], sink_logits[1], size=(B, S, Hq)).astype(np.float32)
+    q[:, :, :, sink_channel] = target / np.float32(scale * amp)
+    qc, dq = quantize_e4m3(q)
+    del q
+    kc, dk = quantize_e4m3(k)
+    del k
+    vc, dv = quantize_e4m3(v)
+    return Fp8Case(qc, kc, vc, dq, dk, dv)
+
+
 def bf16_gaussian_case(B, Hq, Hkv, S, Dqk, Dv, seeds=(20, 21, 22)) -> Bf16Case:
     """Gaussian Q, K, V rounded to bf16."""
     return Bf16Case(to_bf16_bits(gaussian((B, S, Hq, Dqk), seeds[0])),
@@ -113,7 +138,7 @@ def bf16_gaussian_case(B, Hq, Hkv, S, Dqk, Dv, seeds=(20, 21, 22)) -> Bf16Case:
                     to_bf16_bits(gaussian((B, S, Hkv, Dv), seeds[2])))
 
 
-#: The five measured configurations, by name.  ``kind`` selects the path.
+#: The measured configurations, by name.  ``kind`` selects the generator and path.
 CONFIGS = {
     "fp8_h2_s256_d128": dict(kind="fp8", B=1, Hq=2, Hkv=2, S=256, Dqk=128, Dv=128,
                              seeds=(0, 1, 2)),
@@ -128,6 +153,9 @@ CONFIGS = {
                                                    Dqk=192, Dv=128, seeds=(40, 41, 42),
                                                    outlier_seed=43, outliers_qk=4, factor=20.0,
                                                    outliers_v=False),
+    # stress input: an attention sink at key 0 (+15..25 nats, varying per row), V mean 1
+    "fp8_sink_h8_s8k_d128": dict(kind="fp8_sink", B=1, Hq=8, Hkv=8, S=8192, Dqk=128, Dv=128,
+                                 seeds=(50, 51, 52)),
 }
 
 
@@ -138,6 +166,9 @@ def make_case(name: str, S: Optional[int] = None, **overrides):
     if S is not None:
         cfg["S"] = S
     kind = cfg.pop("kind")
+    if kind == "fp8_sink":
+        return fp8_sink_case(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["Dqk"], cfg["Dv"],
+                             seeds=cfg["seeds"])
     if kind == "bf16":
         return bf16_gaussian_case(cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["S"], cfg["Dqk"],
                                   cfg["Dv"], seeds=cfg["seeds"])
