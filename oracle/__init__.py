@@ -79,6 +79,10 @@ def _load():
                                           ctypes.c_double, *shape, ctypes.c_double, i64p,
                                           ctypes.c_int64, ctypes.c_double, dp, dp]
         lib.oracle_emul_exact_fp8.argtypes = lib.oracle_emul_leanp.argtypes
+        lib.oracle_quantize_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.POINTER(ctypes.c_float)]
+        lib.oracle_quantize_e4m3.restype = ctypes.c_int
         lib.oracle_emul_bf16.argtypes = [u8, u8, u8, *shape, ctypes.c_double, i64p,
                                          ctypes.c_int64, dp]
         for f in ("oracle_ref_fp64", "oracle_ref_fp64_bf16", "oracle_emul_leanp",
@@ -269,3 +273,28 @@ def emul_bf16(q, k, v, scale=None, rows=None):
     if rc:
         raise ValueError("oracle_emul_bf16: bad arguments")
     return _finish(out, r, shape)
+
+
+def quantize_e4m3(x, rotate: bool):
+    """Per-tensor e4m3 quantisation of Q or K, optionally after the Hadamard
+    rotation of every head vector (definition in oracle.c; [ART-MTP] "How
+    accurate is ZYFA's FP8 attention?").  ``x`` is float32, or uint16 bf16
+    bits, with the head dimension last (128 or 192).  Returns ``(codes,
+    descale)``: uint8 codes of x's shape and the fp32 descale."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        is_f32 = 1
+    elif x.dtype == np.uint16:
+        is_f32 = 0
+    else:
+        raise TypeError("x must be float32 or uint16 bf16 bits")
+    D = x.shape[-1]
+    n_vec = x.size // D
+    codes = np.empty(x.shape, dtype=np.uint8)
+    ds = ctypes.c_float()
+    rc = lib.oracle_quantize_e4m3(x.ctypes.data_as(ctypes.c_void_p), is_f32, n_vec, D, int(bool(rotate)),
+                                  codes.ctypes.data_as(ctypes.c_void_p), ctypes.byref(ds))
+    if rc:
+        raise ValueError("oracle_quantize_e4m3: bad arguments")
+    return codes, float(ds.value)

@@ -436,3 +436,92 @@ int oracle_leanp_code(double x) { return leanp_code(x); }
 
 int oracle_leanp_C(void) { return LEANP_C; }
 int oracle_leanp_T(void) { return LEANP_T; }
+
+/* ---------------------------------------------------------------------------
+ * Quantisation of Q or K to per-tensor e4m3, optionally after a Hadamard
+ * rotation of every head vector ([ART-MTP] "How accurate is ZYFA's FP8
+ * attention?": most FP8 error comes from quantising Q, K and V, and a Hadamard
+ * rotation of Q and K roughly halves it; the product Q K^T is unchanged by a
+ * common orthogonal rotation).
+ *
+ * Definition (every step in fp32, the precision in which the codes are
+ * decided on the GPU):
+ *   x: n_vec vectors of D elements (bf16 bits or fp32), D in {128, 192}.
+ *   rotate = 0: y = x.
+ *   rotate = 1: y = the unnormalised Walsh-Hadamard transform of x in blocks
+ *     of hb elements (hb = 128 for D = 128; three blocks of 64 for D = 192).
+ *     Butterfly stages h = 1, 2, 4, ..., hb/2; in each, every pair (i, i+h)
+ *     with i mod 2h < h becomes (x_i + x_{i+h}, x_i - x_{i+h}).
+ *   amax = max |y| over the whole tensor; sc = 448 / amax (1 if amax = 0).
+ *   code = e4m3 round-to-nearest-even of the fp32 product y * sc, saturated
+ *     to +-448, keeping the sign of zero.
+ *   descale = (amax / 448) * norm with norm = 1/sqrt(hb) (1 unrotated;
+ *     amax = 0 gives 1 * norm), so dec(code) * descale approximates the
+ *     orthonormal rotation of x.
+ * ------------------------------------------------------------------------- */
+
+/* e4m3 code of an fp32 value: round to nearest even, saturate, keep the sign. */
+static uint8_t e4m3_code_of(float v) {
+  const double r = round_format((double)v, 3, -6, 448.0);
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs(r);
+  if (a == 0.0) return sign;
+  int e2;
+  frexp(a, &e2); /* a = f * 2^e2, f in [0.5, 1) */
+  int lead = e2 - 1;
+  unsigned E, M;
+  if (lead < -6) { /* subnormal: a = M * 2^-9 */
+    E = 0;
+    M = (unsigned)(a / ldexp(1.0, -9));
+  } else {
+    E = (unsigned)(lead + 7);
+    M = (unsigned)(a / ldexp(1.0, lead) * 8.0) - 8u;
+  }
+  return (uint8_t)(sign | (E << 3) | M);
+}
+
+static float in_f32(const void *x, int x_is_f32, int64_t idx) {
+  if (x_is_f32) return ((const float *)x)[idx];
+  uint32_t bits = (uint32_t)((const uint16_t *)x)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return f;
+}
+
+static void rotate_vec(float *y, int D) {
+  const int hb = D == 192 ? 64 : D;
+  for (int base = 0; base < D; base += hb)
+    for (int h = 1; h < hb; h *= 2)
+      for (int i = 0; i < hb; ++i)
+        if ((i % (2 * h)) < h) {
+          const float a = y[base + i], b = y[base + i + h];
+          y[base + i] = a + b;
+          y[base + i + h] = a - b;
+        }
+}
+
+int oracle_quantize_e4m3(const void *x, int x_is_f32, int64_t n_vec, int D, int rotate,
+                         uint8_t *codes, float *descale) {
+  if (!x || !codes || !descale || n_vec < 0 || (D != 128 && D != 192)) return ORACLE_BAD_ARG;
+  float amax = 0.0f;
+  float y[192];
+  for (int64_t v = 0; v < n_vec; ++v) {
+    for (int d = 0; d < D; ++d) y[d] = in_f32(x, x_is_f32, v * D + d);
+    if (rotate) rotate_vec(y, D);
+    for (int d = 0; d < D; ++d)
+      if (fabsf(y[d]) > amax) amax = fabsf(y[d]);
+  }
+  const float sc = amax > 0.0f ? 448.0f / amax : 1.0f;
+  for (int64_t v = 0; v < n_vec; ++v) {
+    for (int d = 0; d < D; ++d) y[d] = in_f32(x, x_is_f32, v * D + d);
+    if (rotate) rotate_vec(y, D);
+    for (int d = 0; d < D; ++d) {
+      const float t = y[d] * sc;
+      codes[v * D + d] = e4m3_code_of(t);
+    }
+  }
+  const float norm = !rotate ? 1.0f : (D == 192 ? 0.125f : 0.0883883476483184405501f);
+  const float base = amax > 0.0f ? amax / 448.0f : 1.0f;
+  *descale = base * norm;
+  return ORACLE_OK;
+}
