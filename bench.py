@@ -406,6 +406,32 @@ def run_sweep(args):
                               "peak_source": peaks["source"], "iterations": n}), flush=True)
         del q, k, v, out
         torch.cuda.empty_cache()
+    # the Q/K quantise pre-pass (optionally Hadamard-rotated) on a bf16 tensor
+    # of the headline Q shape: HBM-bound, reads x twice, writes 1 byte/element
+    x = torch.randn((1, 32768, 32, 128), device=dev).to(torch.bfloat16)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    ds = torch.empty(1, dtype=torch.float32, device=dev)
+    for rot in (False, True):
+        fn = lambda: fa.attn_quantize_fp8(x, hadamard=rot, codes=codes, descale=ds)
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        n = args.steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        alg = x.numel() * 3  # read x once (bf16) + write the codes
+        moved = x.numel() * 5  # the two passes over x + the codes
+        print(json.dumps({"workload": "quantize_bf16_s32k_h32_d128", "path":
+                          "hadamard" if rot else "plain", "ms": ms,
+                          "gbs_algorithmic": alg / (ms * 1e-3) / 1e9,
+                          "gbs_moved": moved / (ms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                          "frac_of_peak_moved": moved / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "iterations": n}), flush=True)
     return 0
 
 

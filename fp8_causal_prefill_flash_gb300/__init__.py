@@ -39,6 +39,8 @@ ATTN_VARIANT_BF16 = 2
 ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 ATTN_FLAG_TEST_STALL_LOADS = 1
+ATTN_IN_BF16 = 0
+ATTN_IN_F32 = 1
 
 HEADER = os.path.join(_build.ROOT, "include", "fp8attn.h")
 LIBRARY_PATH = _build.SO
@@ -75,8 +77,9 @@ def load_library():
         lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
         lib.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
                                     vp, vp]
+        lib.attn_quantize_fp8.argtypes = [vp, i, vp, vp, i, i, i, i, i, vp]
         for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
-                     "attn_launches_per_call", "attn_api_version"):
+                     "attn_quantize_fp8", "attn_launches_per_call", "attn_api_version"):
             getattr(lib, name).restype = ctypes.c_int
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -199,3 +202,33 @@ def attn_fwd_ex(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None
         _raise(st, "attn_fwd_ex")
         return out
     return out, st
+
+
+def attn_quantize_fp8(x, hadamard=False, codes=None, descale=None):
+    """Per-tensor e4m3 quantisation of Q or K (``attn_quantize_fp8`` of the C
+    ABI), optionally after the Hadamard rotation of every head vector; rotate
+    Q and K alike.  ``x`` is a CUDA bf16 or fp32 tensor [B, S, H, D], D in
+    {128, 192}.  Returns ``(codes, descale)``: uint8 e4m3 codes of x's shape and
+    a one-element fp32 tensor, ready for :func:`attn_fwd_fp8`."""
+    lib = load_library()
+    if not x.is_cuda or x.dim() != 4 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [B, S, H, D]")
+    if x.dtype == torch.bfloat16:
+        in_dtype = ATTN_IN_BF16
+    elif x.dtype == torch.float32:
+        in_dtype = ATTN_IN_F32
+    else:
+        raise ValueError("x must be bfloat16 or float32")
+    B, S, H, D = x.shape
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if descale is None:
+        descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if codes.shape != x.shape or codes.dtype != torch.uint8 or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 tensor of x's shape")
+    if descale.dtype != torch.float32 or descale.numel() != 1:
+        raise ValueError("descale must be a one-element float32 tensor")
+    st = lib.attn_quantize_fp8(_ptr(x), in_dtype, _ptr(codes), _ptr(descale), B, S, H, D,
+                               int(bool(hadamard)), _stream_handle())
+    _raise(st, "attn_quantize_fp8")
+    return codes, descale

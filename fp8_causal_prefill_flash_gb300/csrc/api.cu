@@ -11,6 +11,7 @@
 
 #include "../../include/fp8attn.h"
 #include "attn_fwd.cuh"
+#include "quant.cuh"
 
 namespace {
 
@@ -231,6 +232,51 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
     default: return "unknown status";
   }
+}
+
+int attn_quantize_fp8(const void* x, int in_dtype, void* codes, float* descale, int B, int S,
+                      int H, int D, int hadamard, void* stream) {
+  if (!x || !codes || !descale) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || (hadamard != 0 && hadamard != 1)) return ATTN_ERR_INVALID_ARG;
+  if (in_dtype != ATTN_IN_BF16 && in_dtype != ATTN_IN_F32) return ATTN_ERR_INVALID_ARG;
+  if (D != 128 && D != 192) return ATTN_ERR_UNSUPPORTED;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x);
+  if ((xa & 15u) != 0 || (reinterpret_cast<uintptr_t>(codes) & 15u) != 0 ||
+      (reinterpret_cast<uintptr_t>(descale) & 3u) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  const long long n_vec = (long long)B * S * H;
+  if (n_vec > (1ll << 40)) return ATTN_ERR_INVALID_ARG;
+  int sms = 0;
+  const int dc = device_check(&sms);
+  if (dc != ATTN_OK) return dc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // a few waves of warps, each taking eight vectors at a time
+  const long long warps = (n_vec + fa8::kQuantVecPerWarp - 1) / fa8::kQuantVecPerWarp;
+  const long long want = (warps * 32 + fa8::kQuantThreads - 1) / fa8::kQuantThreads;
+  const int grid = (int)(want < 8ll * sms ? want : 8ll * sms);
+  const float norm = !hadamard ? 1.0f : (D == 192 ? 0.125f : 0.0883883476483184405501f);
+  if (cudaMemsetAsync(descale, 0, sizeof(float), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool f32 = in_dtype == ATTN_IN_F32;
+  uint8_t* c = static_cast<uint8_t*>(codes);
+  if (D == 128) {
+    if (f32) {
+      fa8::quant_amax_kernel<128, true><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale);
+      fa8::quant_codes_kernel<128, true><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale, c);
+    } else {
+      fa8::quant_amax_kernel<128, false><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale);
+      fa8::quant_codes_kernel<128, false><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale, c);
+    }
+  } else {
+    if (f32) {
+      fa8::quant_amax_kernel<192, true><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale);
+      fa8::quant_codes_kernel<192, true><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale, c);
+    } else {
+      fa8::quant_amax_kernel<192, false><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale);
+      fa8::quant_codes_kernel<192, false><<<grid, fa8::kQuantThreads, 0, s>>>(x, n_vec, hadamard, descale, c);
+    }
+  }
+  fa8::quant_finish_kernel<<<1, 1, 0, s>>>(descale, norm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_launches_per_call(void) { return 1; }

@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 1
+#define FP8ATTN_API_VERSION 2
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -133,6 +133,36 @@ const char* attn_status_string(int status);
 /* Number of kernel launches one call makes (1 for every supported shape;
  * 0 when S == 0 or B == 0 is rejected).  Lets callers count launches. */
 int attn_launches_per_call(void);
+
+/* Input element type for attn_quantize_fp8. */
+typedef enum { ATTN_IN_BF16 = 0, ATTN_IN_F32 = 1 } attn_in_dtype;
+
+/*
+ * Per-tensor e4m3 quantisation of Q or K for attn_fwd_fp8, optionally after a
+ * Hadamard rotation of every head vector ("Zyphra ZYFA: FP8 FlashAttention for
+ * AMD MI355X", "How accurate is ZYFA's FP8 attention?": most FP8 error comes
+ * from quantising the inputs, and rotating Q and K roughly halves it).  Q and
+ * K must be rotated alike (both or neither): Q K^T is unchanged by a common
+ * orthogonal rotation, V is never rotated.
+ *   x          device pointer, [B, S, H, D] bf16 or fp32 (in_dtype), 16-byte
+ *              aligned; finite values
+ *   codes      device pointer, e4m3 [B, S, H, D], 16-byte aligned (written)
+ *   descale    device pointer to one fp32 (written): dec(code) * descale
+ *              approximates x (rotated: its orthonormal rotation)
+ *   D          128 or 192
+ *   hadamard   0: no rotation.  1: unnormalised Walsh-Hadamard transform of
+ *              each head vector, in one block of 128 (D = 128) or in three
+ *              blocks of 64 (D = 192); the normalisation 1/sqrt(block) goes
+ *              into descale
+ * Arithmetic (fp32 throughout): y = x or its transform (butterfly stages
+ * h = 1, 2, 4, ...; pair (i, i+h) -> (y_i + y_{i+h}, y_i - y_{i+h})),
+ * amax = max|y|, code = e4m3 round-to-nearest-even(y * 448/amax), saturated;
+ * descale = (amax/448) * norm (amax = 0: norm).  Three kernel launches and one
+ * 4-byte memset on `stream`; the descale word holds amax between them, so no
+ * other memory is used.  Returns an attn_status.
+ */
+int attn_quantize_fp8(const void* x, int in_dtype, void* codes, float* descale, int B, int S,
+                      int H, int D, int hadamard, void* stream);
 
 /* Library ABI version (FP8ATTN_API_VERSION of the build). */
 int attn_api_version(void);

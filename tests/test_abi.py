@@ -17,14 +17,15 @@ def lib():
 def test_header_declares_the_entry_points():
     names = fa.declared_functions()
     for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
-              "attn_status_string", "attn_launches_per_call", "attn_api_version"):
+              "attn_quantize_fp8", "attn_status_string", "attn_launches_per_call",
+              "attn_api_version"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 1
+    assert lib.attn_api_version() == 2
     assert lib.attn_launches_per_call() == 1
 
 
@@ -78,3 +79,18 @@ def test_product_entry_points_check_arguments(lib):
         fa.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd_bf16(P, P, P, P, 1, 2, 2, 128, 192, 128, 1, None) == \
         fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_quantize_argument_errors(lib):
+    """Host-side validation of attn_quantize_fp8 runs before any device access."""
+    vp = ctypes.c_void_p
+    q = lib.attn_quantize_fp8
+    assert q(None, 0, P, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG   # null x
+    assert q(P, 2, P, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG      # dtype
+    assert q(P, 0, P, P, 0, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG      # B = 0
+    assert q(P, 0, P, P, 1, 1, 1, 128, 2, None) == fa.ATTN_ERR_INVALID_ARG      # hadamard
+    assert q(P, 0, P, P, 1, 1, 1, 64, 0, None) == fa.ATTN_ERR_UNSUPPORTED       # D
+    assert q(MIS, 0, P, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG    # x alignment
+    assert q(vp(0x10008), 0, P, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG  # x needs 16 B
+    assert q(P, 0, vp(0x10004), P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG  # codes 16 B
+    assert q(P, 0, MIS, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG    # codes alignment
