@@ -105,6 +105,52 @@ def load_peaks():
             "source": "fallback"}
 
 
+# --------------------------------------------------------------------------- energy
+class EnergyMeter:
+    """GPU energy from NVML's total-energy counter (millijoules since the
+    driver loaded), read through ctypes from the driver's NVML library.
+    ``read_mj`` returns None when NVML, the device or the counter is missing.
+    ``nvml`` may be given an object with the same three calls (tests)."""
+
+    def __init__(self, gpu_uuid=None, nvml=None):
+        self.handle = None
+        self.nvml = nvml
+        try:
+            if self.nvml is None:
+                import ctypes
+                lib = ctypes.CDLL("libnvidia-ml.so.1")
+                if lib.nvmlInit_v2() != 0:
+                    return
+                self.nvml = lib
+            import ctypes
+            h = ctypes.c_void_p()
+            if gpu_uuid:
+                rc = self.nvml.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(h))
+            else:
+                rc = self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h))
+            if rc == 0:
+                self.handle = h
+        except (OSError, AttributeError):
+            self.handle = None
+
+    def read_mj(self):
+        if self.handle is None:
+            return None
+        import ctypes
+        e = ctypes.c_ulonglong(0)
+        if self.nvml.nvmlDeviceGetTotalEnergyConsumption(self.handle, ctypes.byref(e)) != 0:
+            return None
+        return int(e.value)
+
+
+def energy_report(mj0, mj1, flops):
+    """Joules between two counter readings and TFLOP per joule (None if unread)."""
+    if mj0 is None or mj1 is None or mj1 <= mj0:
+        return None
+    j = (mj1 - mj0) / 1000.0
+    return {"joules": j, "tflop_per_joule": flops / 1e12 / j, "source": "NVML total energy counter"}
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) taken while the timed region runs."""
@@ -162,6 +208,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
+                "power_w_median": statistics.median(power) if power else None,
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
@@ -271,12 +318,15 @@ def run_ours(args, rank, world, local_rank):
     except Exception:
         uuid = None
     clocks = ClockSampler(uuid)
+    meter = EnergyMeter(uuid)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    e_start = meter.read_mj()
     ms = timed(step, args.steps, 0)
+    e_end = meter.read_mj()
     clk = clocks.stop()
     if args.leanp_only:
         if rank == 0:
@@ -326,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
                     "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h)},
             "gpu_launches": args.steps,
-            "clocks": clk}
+            "clocks": clk,
+            "energy": energy_report(e_start, e_end, F * args.steps)}
 
     if rank == 0 and world == 1 and not args.no_cpu:
         # CPU oracle on a bounded sample of the same workload, and the accuracy
@@ -435,6 +486,61 @@ def run_sweep(args):
     return 0
 
 
+def run_clock_study(args):
+    """Sustained runs (about `--study-seconds` each) of Lean-P and the ablation
+    on inputs of different statistics, with the SM clock, the power and the
+    energy sampled throughout: one JSON line per (input, path)."""
+    import torch
+
+    import fp8_causal_prefill_flash_gb300 as fa
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+    fa.build()
+    fa.load_library()
+    dev = torch.device("cuda", 0)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    meter = EnergyMeter(uuid)
+    for name in ("fp8_h32_s32k_d128", "fp8_gqa_h32_8_s16k_d128_outliers", "fp8_sink_h8_s8k_d128"):
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        F = causal_flops(B, Hq, S, Dqk, Dv)
+        q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+        d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+        out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+        for path, fn in (("leanp", lambda: fa.attn_fwd_fp8(q, k, v, *d, out=out)),
+                         ("exact_fp8_ablation", lambda: fa.attn_fwd_fp8_exact(q, k, v, *d, out=out))):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            n = max(1, int(args.study_seconds * 1000.0 / max(e0.elapsed_time(e1), 1e-3)))
+            clocks = ClockSampler(uuid)
+            clocks.start()
+            time.sleep(0.3)
+            mj0 = meter.read_mj()
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            mj1 = meter.read_mj()
+            clk = clocks.stop()
+            ms = e0.elapsed_time(e1) / n
+            print(json.dumps({"workload": name, "path": path, "calls": n, "ms": ms,
+                              "tflops_causal": F / (ms * 1e-3) / 1e12, "clocks": clk,
+                              "energy": energy_report(mj0, mj1, F * n)}), flush=True)
+        del q, k, v, out
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -456,6 +562,9 @@ def main():
                     help="time only the Lean-P kernel and print a short line (profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every path on every configuration, one JSON line each")
+    ap.add_argument("--clock-study", action="store_true",
+                    help="sustained runs per input distribution: SM clock, power, energy")
+    ap.add_argument("--study-seconds", type=float, default=3.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -468,6 +577,8 @@ def main():
         return run_reference(args, rank, world)
     if args.sweep:
         return run_sweep(args)
+    if args.clock_study:
+        return run_clock_study(args)
     if world > 1:
         import torch
         import torch.distributed as dist

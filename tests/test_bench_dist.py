@@ -54,3 +54,33 @@ def test_reference_arm_other_ranks_exit_without_work():
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+class _FakeNvml:
+    """Stands in for the driver's NVML library: a counter that advances by
+    1500 mJ per read."""
+
+    def __init__(self):
+        self.mj = 10_000
+
+    def nvmlDeviceGetHandleByUUID(self, uuid, handle_ref):
+        return 0 if uuid.startswith(b"GPU-") else 1
+
+    def nvmlDeviceGetHandleByIndex_v2(self, index, handle_ref):
+        return 0
+
+    def nvmlDeviceGetTotalEnergyConsumption(self, handle, energy_ref):
+        energy_ref._obj.value = self.mj
+        self.mj += 1500
+        return 0
+
+
+def test_energy_meter_and_report():
+    import bench
+    m = bench.EnergyMeter("GPU-1234", nvml=_FakeNvml())
+    a, b = m.read_mj(), m.read_mj()
+    rep = bench.energy_report(a, b, 3e12)
+    assert rep["joules"] == 1.5 and abs(rep["tflop_per_joule"] - 2.0) < 1e-12
+    # an unknown device or an unread counter gives no report, not an error
+    assert bench.EnergyMeter("bad", nvml=_FakeNvml()).read_mj() is None
+    assert bench.energy_report(None, 5, 1.0) is None and bench.energy_report(5, 5, 1.0) is None
