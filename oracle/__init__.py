@@ -79,6 +79,19 @@ def _load():
                                           ctypes.c_double, *shape, ctypes.c_double, i64p,
                                           ctypes.c_int64, ctypes.c_double, dp, dp]
         lib.oracle_emul_exact_fp8.argtypes = lib.oracle_emul_leanp.argtypes
+        dp = ctypes.POINTER(ctypes.c_double)
+        vp = ctypes.c_void_p
+        lib.oracle_ref_fp64_ex.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, dp, ctypes.c_int,
+                                           ctypes.c_int, *shape, ctypes.c_double, i64p,
+                                           ctypes.c_int64, dp, dp]
+        lib.oracle_emul_leanp_ex.argtypes = [vp, vp, vp, dp, dp, dp, ctypes.c_int, ctypes.c_int,
+                                             *shape, ctypes.c_double, i64p, ctypes.c_int64,
+                                             ctypes.c_double, dp, dp, dp]
+        lib.oracle_emul_exact_ex.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, dp, ctypes.c_int,
+                                             ctypes.c_int, *shape, ctypes.c_double, i64p,
+                                             ctypes.c_int64, ctypes.c_double, dp, dp, dp]
+        for fn in ("oracle_ref_fp64_ex", "oracle_emul_leanp_ex", "oracle_emul_exact_ex"):
+            getattr(lib, fn).restype = ctypes.c_int
         lib.oracle_quantize_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                              ctypes.POINTER(ctypes.c_float)]
@@ -298,3 +311,56 @@ def quantize_e4m3(x, rotate: bool):
     if rc:
         raise ValueError("oracle_quantize_e4m3: bad arguments")
     return codes, float(ds.value)
+
+
+def _descales(dq, dk, dv, B, Hkv):
+    """One value each, or [B, Hkv] arrays (per batch and kv head)."""
+    arrs = [np.ascontiguousarray(np.asarray(d, dtype=np.float64).reshape(-1)) for d in (dq, dk, dv)]
+    sizes = {a.size for a in arrs}
+    if sizes == {1}:
+        return arrs, 0
+    if sizes == {B * Hkv}:
+        return arrs, 1
+    raise ValueError("descales must be scalars or [B, Hkv] arrays")
+
+
+def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, causal=True,
+              kappa=DEFAULT_KAPPA):
+    """All definitions with every option (non-causal, per-(batch, kv head)
+    descales) and the per-row log-sum-exp.  ``path`` is "ref" (fp64 on e4m3
+    codes), "ref_bf16", "leanp", "exact_fp8" or "bf16".  Returns ``(out, amb,
+    lse)``: out [B,S,Hq,Dv] or (n, Dv) for ``rows``; amb per row (None for the
+    reference and BF16 paths); lse per row, natural log of the row sum (the
+    unnormalised weights of that path), shaped [B,Hq,S] or (n,)."""
+    lib = _load()
+    bf16 = path in ("ref_bf16", "bf16")
+    dt = np.uint16 if bf16 else np.uint8
+    q, k, v = (np.ascontiguousarray(a, dtype=dt) for a in (q, k, v))
+    shape = _shape(q, k, v)
+    B, Hq, Hkv = shape[0], shape[1], shape[2]
+    (aq, ak, av), per = _descales(dq, dk, dv, B, Hkv)
+    r, n = _rows(rows, shape)
+    out = np.empty((n, shape[5]), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    amb = None if path in ("ref", "ref_bf16", "bf16") else np.empty((n,), dtype=np.float64)
+    rp = None if r is None else _ptr(r)
+    args = (_dptr(aq), _dptr(ak), _dptr(av), per, int(bool(causal)), *shape,
+            _scale(scale, shape[4]), rp, n)
+    if path in ("ref", "ref_bf16"):
+        rc = lib.oracle_ref_fp64_ex(_ptr(q), _ptr(k), _ptr(v), int(bf16), *args, _dptr(out), _dptr(lse))
+    elif path == "leanp":
+        rc = lib.oracle_emul_leanp_ex(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
+                                      _dptr(amb), _dptr(lse))
+    elif path in ("exact_fp8", "bf16"):
+        rc = lib.oracle_emul_exact_ex(_ptr(q), _ptr(k), _ptr(v), int(bf16), *args, float(kappa),
+                                      _dptr(out), None if amb is None else _dptr(amb), _dptr(lse))
+    else:
+        raise ValueError(path)
+    if rc:
+        raise ValueError(f"oracle {path}: bad arguments")
+    if r is None:
+        out = out.reshape(B, shape[3], Hq, shape[5])
+        lse = lse.reshape(B, shape[3], Hq).transpose(0, 2, 1).copy()
+        if amb is not None:
+            amb = amb.reshape(B, shape[3], Hq)
+    return out, amb, lse

@@ -27,6 +27,9 @@
  *                           (the "hardware exponential" column of [ART-MTP]
  *                           "How does ZYFA compare with other attention kernels?").
  *   oracle_emul_bf16     -- the exact-softmax BF16 path ([ART-MTP] "TL;DR").
+ *   The *_ex forms take the options of a flash_attn_func-style call ([ART-MTP]
+ *   "TL;DR" names that interface): causal or not, descales per (batch, kv
+ *   head) or per tensor, and a per-row log-sum-exp of the path's own row sum.
  *
  * Readings where the articles are silent (each is listed in the design doc):
  *   - e4m3 is OCP E4M3 (bias 7, max 448, S.1111.111 = NaN, no infinities).
@@ -116,6 +119,24 @@ typedef struct {
   int B, Hq, Hkv, S, Dqk, Dv;
 } shape_t;
 
+/* Options common to the attention definitions: descales (one value, or one
+ * per (batch, kv head) in [B, Hkv] order), the causal flag (keys j <= i, else
+ * all S keys) and an optional per-row log-sum-exp output. */
+typedef struct {
+  const double *dq, *dk, *dv;
+  int per_bkv;
+  int causal;
+} opts_t;
+
+static double dsc(const double *a, const opts_t *o, const shape_t *sh, int b, int h) {
+  if (!o->per_bkv) return a[0];
+  int g = (int)(((int64_t)h * sh->Hkv) / sh->Hq);
+  return a[(int64_t)b * sh->Hkv + g];
+}
+
+/* Number of keys row i attends to. */
+static int keys_of(const opts_t *o, const shape_t *sh, int i) { return o->causal ? i + 1 : sh->S; }
+
 static int check_shape(const shape_t *sh) {
   if (sh->B < 1 || sh->Hq < 1 || sh->Hkv < 1 || sh->S < 0 || sh->Dqk < 1 || sh->Dv < 1)
     return ORACLE_BAD_ARG;
@@ -181,36 +202,41 @@ static double v_val(const void *v, const shape_t *sh, int is_bf16, int b, int h,
 }
 
 /* ---------------------------------------------------------------------------
- * O-1: fp64 causal attention on the dequantized inputs.
- *   z_ij = scale * <dq*q_i, dk*k_j>  (j <= i),  w = softmax_j(z_i.),
- *   out_i = sum_j w_ij * dv * v_j.
+ * O-1: fp64 attention on the dequantized inputs.
+ *   z_ij = scale * <dq*q_i, dk*k_j>  (j <= i if causal, else all j < S),
+ *   w = softmax_j(z_i.),  out_i = sum_j w_ij * dv * v_j,
+ *   lse_i = ln sum_j exp(z_ij)  (natural log of the unnormalised row sum).
  * ------------------------------------------------------------------------- */
-static int ref_fp64_impl(const void *q, const void *k, const void *v, int is_bf16, double dq,
-                         double dk, double dv, shape_t sh, double scale, const int64_t *rows,
-                         int64_t nrows, double *out) {
+static int ref_fp64_impl(const void *q, const void *k, const void *v, int is_bf16, opts_t o,
+                         shape_t sh, double scale, const int64_t *rows, int64_t nrows,
+                         double *out, double *lse) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;
     row_at(&sh, rows, r, &b, &h, &i);
-    double *z = (double *)malloc(sizeof(double) * (size_t)(i + 1));
+    const int n = keys_of(&o, &sh, i);
+    const double dqk = dsc(o.dq, &o, &sh, b, h) * dsc(o.dk, &o, &sh, b, h);
+    const double dv = dsc(o.dv, &o, &sh, b, h);
+    double *z = (double *)malloc(sizeof(double) * (size_t)n);
     double m = -INFINITY;
-    for (int j = 0; j <= i; ++j) {
+    for (int j = 0; j < n; ++j) {
       double s;
       dot_row(q, k, &sh, is_bf16, b, h, i, j, &s, NULL);
-      z[j] = scale * (dq * dk * s);
+      z[j] = scale * (dqk * s);
       if (z[j] > m) m = z[j];
     }
     double L = 0.0;
-    for (int j = 0; j <= i; ++j) {
+    for (int j = 0; j < n; ++j) {
       z[j] = exp(z[j] - m);
       L += z[j];
     }
     for (int d = 0; d < sh.Dv; ++d) {
       double acc = 0.0;
-      for (int j = 0; j <= i; ++j) acc += z[j] * (dv * v_val(v, &sh, is_bf16, b, h, j, d));
+      for (int j = 0; j < n; ++j) acc += z[j] * (dv * v_val(v, &sh, is_bf16, b, h, j, d));
       out[r * sh.Dv + d] = acc / L;
     }
+    if (lse) lse[r] = m + log(L);
     free(z);
   }
   return ORACLE_OK;
@@ -220,14 +246,32 @@ int oracle_ref_fp64(const uint8_t *q, const uint8_t *k, const uint8_t *v, double
                     double dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
                     const int64_t *rows, int64_t nrows, double *out) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
-  return ref_fp64_impl(q, k, v, 0, dq, dk, dv, sh, scale, rows, nrows, out);
+  opts_t o = {&dq, &dk, &dv, 0, 1};
+  return ref_fp64_impl(q, k, v, 0, o, sh, scale, rows, nrows, out, NULL);
 }
 
 int oracle_ref_fp64_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
                          int Hkv, int S, int Dqk, int Dv, double scale, const int64_t *rows,
                          int64_t nrows, double *out) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
-  return ref_fp64_impl(q, k, v, 1, 1.0, 1.0, 1.0, sh, scale, rows, nrows, out);
+  const double one = 1.0;
+  opts_t o = {&one, &one, &one, 0, 1};
+  return ref_fp64_impl(q, k, v, 1, o, sh, scale, rows, nrows, out, NULL);
+}
+
+/* General form: is_bf16 selects bf16 inputs (descales then ignored, pass
+ * NULL); dq/dk/dv hold one value or B*Hkv values (per_bkv); lse optional. */
+int oracle_ref_fp64_ex(const void *q, const void *k, const void *v, int is_bf16,
+                       const double *dq, const double *dk, const double *dv, int per_bkv,
+                       int causal, int B, int Hq, int Hkv, int S, int Dqk, int Dv,
+                       double scale, const int64_t *rows, int64_t nrows, double *out,
+                       double *lse) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  const double one = 1.0;
+  opts_t o = {is_bf16 ? &one : dq, is_bf16 ? &one : dk, is_bf16 ? &one : dv,
+              is_bf16 ? 0 : per_bkv, causal};
+  if (!o.dq || !o.dk || !o.dv) return ORACLE_BAD_ARG;
+  return ref_fp64_impl(q, k, v, is_bf16, o, sh, scale, rows, nrows, out, lse);
 }
 
 /* ---------------------------------------------------------------------------
@@ -241,7 +285,7 @@ int oracle_ref_fp64_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v
  * scaled by a power of two before rounding, the scale is removed inside the
  * P.V product, and the row is divided by the sum of the ROUNDED probabilities.
  *
- * Per row i and block beta (unmasked keys j <= i only):
+ * Per row i and block beta (unmasked keys: j <= i, or all j < S non-causal):
  *   u_j   = 8 * lambda * s_j                                  (code units)
  *   e     = ceil(max_{j in beta} u_j / 8)                     (block exponent)
  *   c_j   = clamp(floor(u_j - 8e + C), 0, 126)                (Lean-P code)
@@ -264,18 +308,18 @@ static int leanp_code(double x) {
   return (int)f;
 }
 
-int oracle_emul_leanp(const uint8_t *q, const uint8_t *k, const uint8_t *v, double dq, double dk,
-                      double dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
-                      const int64_t *rows, int64_t nrows, double kappa, double *out,
-                      double *amb) {
-  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts_t o, shape_t sh,
+                      double scale, const int64_t *rows, int64_t nrows, double kappa, double *out,
+                      double *amb, double *lse) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
-  const double lam = scale * dq * dk / log(2.0); /* log2(e) * scale * dq * dk */
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;
     row_at(&sh, rows, r, &b, &h, &i);
-    int n = i + 1;
+    /* log2(e) * scale * dq * dk */
+    const double lam = scale * dsc(o.dq, &o, &sh, b, h) * dsc(o.dk, &o, &sh, b, h) / log(2.0);
+    const double dv = dsc(o.dv, &o, &sh, b, h);
+    int n = keys_of(&o, &sh, i);
     int nblk = (n + LEANP_BLOCK - 1) / LEANP_BLOCK;
     double *u = (double *)malloc(sizeof(double) * (size_t)n);
     double *du = (double *)malloc(sizeof(double) * (size_t)n);
@@ -338,12 +382,34 @@ int oracle_emul_leanp(const uint8_t *q, const uint8_t *k, const uint8_t *v, doub
       out[r * sh.Dv + d] = dv * acc / L;
     }
     if (amb) amb[r] = dmass / L;
+    /* the rounded row sum in absolute units: sum_j w_j * 2^E ~ sum_j e^(z_j) */
+    if (lse) lse[r] = log(L) + E * log(2.0);
     free(u);
     free(du);
     free(w);
     free(eb);
   }
   return ORACLE_OK;
+}
+
+int oracle_emul_leanp(const uint8_t *q, const uint8_t *k, const uint8_t *v, double dq, double dk,
+                      double dv, int B, int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
+                      const int64_t *rows, int64_t nrows, double kappa, double *out,
+                      double *amb) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  opts_t o = {&dq, &dk, &dv, 0, 1};
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, NULL);
+}
+
+int oracle_emul_leanp_ex(const uint8_t *q, const uint8_t *k, const uint8_t *v, const double *dq,
+                         const double *dk, const double *dv, int per_bkv, int causal, int B,
+                         int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
+                         const int64_t *rows, int64_t nrows, double kappa, double *out,
+                         double *amb, double *lse) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  if (!dq || !dk || !dv) return ORACLE_BAD_ARG;
+  opts_t o = {dq, dk, dv, per_bkv, causal};
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse);
 }
 
 /* ---------------------------------------------------------------------------
@@ -359,16 +425,17 @@ int oracle_emul_leanp(const uint8_t *q, const uint8_t *k, const uint8_t *v, doub
  * amb[r] (FP8 only): mass that may move when p_j lies within its fp32
  * evaluation band of an e4m3 rounding midpoint.
  * ------------------------------------------------------------------------- */
-static int exact_impl(const void *q, const void *k, const void *v, int is_bf16, double dq,
-                      double dk, double dv, shape_t sh, double scale, const int64_t *rows,
-                      int64_t nrows, double kappa, double *out, double *amb) {
+static int exact_impl(const void *q, const void *k, const void *v, int is_bf16, opts_t o,
+                      shape_t sh, double scale, const int64_t *rows, int64_t nrows, double kappa,
+                      double *out, double *amb, double *lse) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
-  const double lam = scale * dq * dk / log(2.0);
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;
     row_at(&sh, rows, r, &b, &h, &i);
-    int n = i + 1;
+    const double lam = scale * dsc(o.dq, &o, &sh, b, h) * dsc(o.dk, &o, &sh, b, h) / log(2.0);
+    const double dv = dsc(o.dv, &o, &sh, b, h);
+    int n = keys_of(&o, &sh, i);
     double *x = (double *)malloc(sizeof(double) * (size_t)n); /* lambda2 * s_j (log2 units) */
     double *dx = (double *)malloc(sizeof(double) * (size_t)n);
     double *O = (double *)calloc((size_t)sh.Dv, sizeof(double));
@@ -408,6 +475,7 @@ static int exact_impl(const void *q, const void *k, const void *v, int is_bf16, 
     }
     for (int d = 0; d < sh.Dv; ++d) out[r * sh.Dv + d] = dv * O[d] / l;
     if (amb) amb[r] = is_bf16 ? 0.0 : dmass / l;
+    if (lse) lse[r] = (m + log2(l)) * log(2.0); /* row sum of the unrounded p */
     free(x);
     free(dx);
     free(O);
@@ -420,14 +488,32 @@ int oracle_emul_exact_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v, 
                           double scale, const int64_t *rows, int64_t nrows, double kappa,
                           double *out, double *amb) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
-  return exact_impl(q, k, v, 0, dq, dk, dv, sh, scale, rows, nrows, kappa, out, amb);
+  opts_t o = {&dq, &dk, &dv, 0, 1};
+  return exact_impl(q, k, v, 0, o, sh, scale, rows, nrows, kappa, out, amb, NULL);
 }
 
 int oracle_emul_bf16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int B, int Hq,
                      int Hkv, int S, int Dqk, int Dv, double scale, const int64_t *rows,
                      int64_t nrows, double *out) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
-  return exact_impl(q, k, v, 1, 1.0, 1.0, 1.0, sh, scale, rows, nrows, 0.0, out, NULL);
+  const double one = 1.0;
+  opts_t o = {&one, &one, &one, 0, 1};
+  return exact_impl(q, k, v, 1, o, sh, scale, rows, nrows, 0.0, out, NULL, NULL);
+}
+
+/* General form of both exact paths (is_bf16: the BF16 path, descales ignored). */
+int oracle_emul_exact_ex(const void *q, const void *k, const void *v, int is_bf16,
+                         const double *dq, const double *dk, const double *dv, int per_bkv,
+                         int causal, int B, int Hq, int Hkv, int S, int Dqk, int Dv,
+                         double scale, const int64_t *rows, int64_t nrows, double kappa,
+                         double *out, double *amb, double *lse) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  const double one = 1.0;
+  opts_t o = {is_bf16 ? &one : dq, is_bf16 ? &one : dk, is_bf16 ? &one : dv,
+              is_bf16 ? 0 : per_bkv, causal};
+  if (!o.dq || !o.dk || !o.dv) return ORACLE_BAD_ARG;
+  return exact_impl(q, k, v, is_bf16, o, sh, scale, rows, nrows, is_bf16 ? 0.0 : kappa, out,
+                    is_bf16 ? NULL : amb, lse);
 }
 
 /* Lean-P code of a single code-unit argument x (exposed for the closed-form

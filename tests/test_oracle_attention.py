@@ -294,3 +294,98 @@ def test_sink_input_block_scale_beats_ablation(oracle_mod):
     e_lp, e_ab = rel_rms(lp, ref), rel_rms(ab, ref)
     assert e_lp < 3e-2
     assert e_lp < 0.3 * e_ab, (e_lp, e_ab)
+
+
+# --- options for flash_attn_func-style calls: non-causal, per-(batch, kv
+# head) descales, log-sum-exp ------------------------------------------------
+
+def _dequant(oracle_mod, c, B, Hkv, dq, dk, dv):
+    """Dequantised q, k, v with per-(b, kv head) descales (GQA groups share)."""
+    Hq = c.q.shape[2]
+    grp = Hq // Hkv
+    q = oracle_mod.e4m3_decode(c.q) * np.repeat(np.asarray(dq).reshape(B, 1, Hkv, 1), grp, 2)
+    k = oracle_mod.e4m3_decode(c.k) * np.asarray(dk).reshape(B, 1, Hkv, 1)
+    v = oracle_mod.e4m3_decode(c.v) * np.asarray(dv).reshape(B, 1, Hkv, 1)
+    return q, k, v
+
+
+def _sdpa(q, k, v, causal, scale):
+    Hq, Hkv = q.shape[2], k.shape[2]
+    kk = torch.from_numpy(np.repeat(k, Hq // Hkv, axis=2)).permute(0, 2, 1, 3)
+    vv = torch.from_numpy(np.repeat(v, Hq // Hkv, axis=2)).permute(0, 2, 1, 3)
+    qq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    out = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, is_causal=causal, scale=scale)
+    s = torch.einsum("bhid,bhjd->bhij", qq, kk) * scale
+    if causal:
+        S = s.shape[-1]
+        s = s.masked_fill(torch.triu(torch.ones(S, S, dtype=torch.bool), 1), float("-inf"))
+    return out.permute(0, 2, 1, 3).numpy(), torch.logsumexp(s, -1).numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_reference_options_match_sdpa_and_logsumexp(oracle_mod, causal):
+    """Non-causal rows, per-(batch, kv head) descales and the log-sum-exp of the
+    fp64 reference against torch's SDPA and logsumexp in fp64."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 70, 32
+    c = wl.fp8_gaussian_case(B, Hq, Hkv, S, D, D, seeds=(81, 82, 83))
+    rng = np.random.default_rng(84)
+    dq, dk, dv = (c.dq * rng.uniform(0.5, 2.0, (B, Hkv)), c.dk * rng.uniform(0.5, 2.0, (B, Hkv)),
+                  c.dv * rng.uniform(0.5, 2.0, (B, Hkv)))
+    scale = 0.21
+    out, _, lse = oracle_mod.attention("ref", c.q, c.k, c.v, dq, dk, dv, scale=scale, causal=causal)
+    want, want_lse = _sdpa(*_dequant(oracle_mod, c, B, Hkv, dq, dk, dv), causal, scale)
+    assert np.max(np.abs(out - want)) < 1e-12
+    assert np.max(np.abs(lse - want_lse)) < 1e-12
+
+
+@pytest.mark.parametrize("path", ["leanp", "exact_fp8"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_per_bkv_descales_equal_per_slice_calls(oracle_mod, path, causal):
+    """Per-(batch, kv head) descales give, slice by slice, what a call on that
+    slice with its scalar descales gives."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 150, 64
+    c = wl.fp8_gaussian_case(B, Hq, Hkv, S, D, D, seeds=(85, 86, 87))
+    rng = np.random.default_rng(88)
+    dq, dk, dv = (rng.uniform(0.005, 0.02, (B, Hkv)) for _ in range(3))
+    out, amb, lse = oracle_mod.attention(path, c.q, c.k, c.v, dq, dk, dv, causal=causal)
+    grp = Hq // Hkv
+    for b in range(B):
+        for g in range(Hkv):
+            sl = lambda a, h0, h1: np.ascontiguousarray(a[b:b + 1, :, h0:h1])
+            o2, a2, l2 = oracle_mod.attention(
+                path, sl(c.q, g * grp, (g + 1) * grp), sl(c.k, g, g + 1), sl(c.v, g, g + 1),
+                dq[b, g], dk[b, g], dv[b, g], causal=causal)
+            assert np.array_equal(out[b:b + 1, :, g * grp:(g + 1) * grp], o2)
+            assert np.array_equal(lse[b:b + 1, g * grp:(g + 1) * grp], l2)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_lse_of_each_path(oracle_mod, causal):
+    """Lean-P's log-sum-exp is the log of the rounded row sum, so it lies in
+    the closed-form element band (2^(-1/8), 1.0607] of the fp64 one (plus the
+    tiny flushed weights); the exact ablation's (unrounded sum) equals it."""
+    c = wl.fp8_gaussian_case(1, 2, 2, 333, 128, 128, seeds=(91, 92, 93))
+    _, _, ref = oracle_mod.attention("ref", c.q, c.k, c.v, c.dq, c.dk, c.dv, causal=causal)
+    _, _, lp = oracle_mod.attention("leanp", c.q, c.k, c.v, c.dq, c.dk, c.dv, causal=causal)
+    _, _, ex = oracle_mod.attention("exact_fp8", c.q, c.k, c.v, c.dq, c.dk, c.dv, causal=causal)
+    d = lp - ref
+    assert d.min() > math.log(2.0 ** (-1.0 / 8.0)) - 1e-6 and d.max() <= math.log(1.0607) + 1e-9
+    assert np.max(np.abs(ex - ref)) < 1e-9
+
+
+def test_noncausal_q_zero_gives_mean_of_all_keys(oracle_mod):
+    S = 200
+    c = wl.fp8_gaussian_case(1, 2, 2, S, 128, 128, seeds=(94, 95, 96))
+    q0 = np.zeros_like(c.q)
+    want = (oracle_mod.e4m3_decode(c.v) * c.dv).mean(axis=1, keepdims=True)
+    for path in ("ref", "leanp", "exact_fp8"):
+        out, _, _ = oracle_mod.attention(path, q0, c.k, c.v, c.dq, c.dk, c.dv, causal=False)
+        assert np.max(np.abs(out - want)) < 1e-12, path
+
+
+def test_bf16_reference_noncausal_matches_sdpa(oracle_mod):
+    b = wl.bf16_gaussian_case(1, 2, 2, 90, 64, 64)
+    out, _, lse = oracle_mod.attention("ref_bf16", b.q, b.k, b.v, causal=False)
+    q, k, v = (oracle_mod.bf16_decode(a) for a in (b.q, b.k, b.v))
+    want, want_lse = _sdpa(q, k, v, False, 1.0 / math.sqrt(64))
+    assert np.max(np.abs(out - want)) < 1e-12 and np.max(np.abs(lse - want_lse)) < 1e-12
