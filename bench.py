@@ -457,6 +457,38 @@ def run_sweep(args):
                               "peak_source": peaks["source"], "iterations": n}), flush=True)
         del q, k, v, out
         torch.cuda.empty_cache()
+    # non-causal calls (flash_attn_func causal=False): every row sees all S keys
+    for name in ("fp8_gqa_h32_8_s16k_d128_outliers", "bf16_gqa_h32_8_s16k_d128"):
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        F = square_flops(B, Hq, S, Dqk, Dv)
+        if name.startswith("fp8"):
+            q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+            d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+            fn = lambda: fa.attn_fwd_full(fa.ATTN_VARIANT_LEANP, q, k, v, *d, causal=False)
+            path, peak = "leanp_noncausal", peaks["bf16_burst"] * FP8_OVER_BF16
+        else:
+            q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                       for a in (case.q, case.k, case.v))
+            fn = lambda: fa.attn_fwd_full(fa.ATTN_VARIANT_BF16, q, k, v, causal=False)
+            path, peak = "bf16_noncausal", peaks["bf16_burst"]
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        n = args.steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        tf = F / (ms * 1e-3) / 1e12
+        print(json.dumps({"workload": name, "path": path, "ms": ms, "tflops": tf,
+                          "flop_count": "2*B*Hq*S^2*(Dqk+Dv) (every pair computed)", "peak": peak,
+                          "frac_of_peak": tf / peak, "iterations": n}), flush=True)
+        del q, k, v
+        torch.cuda.empty_cache()
     # the Q/K quantise pre-pass (optionally Hadamard-rotated) on a bf16 tensor
     # of the headline Q shape: HBM-bound, reads x twice, writes 1 byte/element
     x = torch.randn((1, 32768, 32, 128), device=dev).to(torch.bfloat16)

@@ -39,6 +39,7 @@ ATTN_VARIANT_BF16 = 2
 ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 ATTN_FLAG_TEST_STALL_LOADS = 1
+ATTN_FLAG_DESCALE_PER_BKV = 2
 ATTN_IN_BF16 = 0
 ATTN_IN_F32 = 1
 
@@ -78,8 +79,11 @@ def load_library():
         lib.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
                                     vp, vp]
         lib.attn_quantize_fp8.argtypes = [vp, i, vp, vp, i, i, i, i, i, vp]
+        lib.attn_fwd_full.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
+                                      i, vp, vp]
         for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
-                     "attn_quantize_fp8", "attn_launches_per_call", "attn_api_version"):
+                     "attn_quantize_fp8", "attn_fwd_full", "attn_launches_per_call",
+                     "attn_api_version"):
             getattr(lib, name).restype = ctypes.c_int
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
@@ -232,3 +236,55 @@ def attn_quantize_fp8(x, hadamard=False, codes=None, descale=None):
                                int(bool(hadamard)), _stream_handle())
     _raise(st, "attn_quantize_fp8")
     return codes, descale
+
+
+def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None, out=None,
+                  out_dtype=ATTN_OUT_BF16, causal=True, softmax_scale=None, return_lse=False,
+                  dev_status=None, flags=0):
+    """The general entry point (``attn_fwd_full`` of the C ABI).  Descales are
+    one-element tensors or [B, Hkv] tensors (one per batch and kv head).
+    Returns ``out``, or ``(out, lse)`` with lse fp32 [B, Hq, S] (natural log of
+    the row's own unnormalised weights)."""
+    lib = load_library()
+    fp8 = variant != ATTN_VARIANT_BF16
+    B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, fp8)
+    if fp8:
+        sizes = {int(t.numel()) for t in (descale_q, descale_k, descale_v)}
+        if sizes == {B * Hkv} and B * Hkv != 1:
+            flags |= ATTN_FLAG_DESCALE_PER_BKV
+        elif sizes != {1}:
+            raise ValueError("descales must be one-element or [B, Hkv] float32 tensors")
+        for name, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+            if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    dtype = torch.float32 if out_dtype == ATTN_OUT_F32 else torch.bfloat16
+    out = _out(out, q, Dv, dtype)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if return_lse else None
+    st = lib.attn_fwd_full(variant, _ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                           _ptr(descale_v), _ptr(out), out_dtype, _ptr(lse), B, Hq, Hkv, S, Dqk,
+                           Dv, int(bool(causal)), float(softmax_scale or 0.0), flags,
+                           _ptr(dev_status), _stream_handle())
+    _raise(st, "attn_fwd_full")
+    return (out, lse) if return_lse else out
+
+
+def flash_attn_fp8_func(q, k, v, q_descale=None, k_descale=None, v_descale=None,
+                        softmax_scale=None, causal=True, return_softmax_lse=False, exact=False):
+    """flash_attn_func-style call on e4m3 inputs (uint8 codes, BSHD): the
+    Lean-P path, or the exact-softmax ablation with ``exact=True``.
+    Descales default to 1; they may be [B, Hkv] tensors."""
+    one = None
+    if q_descale is None or k_descale is None or v_descale is None:
+        one = torch.ones(1, dtype=torch.float32, device=q.device)
+    return attn_fwd_full(ATTN_VARIANT_EXACT_FP8 if exact else ATTN_VARIANT_LEANP, q, k, v,
+                         one if q_descale is None else q_descale,
+                         one if k_descale is None else k_descale,
+                         one if v_descale is None else v_descale,
+                         causal=causal, softmax_scale=softmax_scale,
+                         return_lse=return_softmax_lse)
+
+
+def flash_attn_bf16_func(q, k, v, softmax_scale=None, causal=True, return_softmax_lse=False):
+    """flash_attn_func-style call on bf16 inputs (exact softmax)."""
+    return attn_fwd_full(ATTN_VARIANT_BF16, q, k, v, causal=causal, softmax_scale=softmax_scale,
+                         return_lse=return_softmax_lse)

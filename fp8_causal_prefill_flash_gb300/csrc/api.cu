@@ -109,8 +109,9 @@ int launch(const Maps& maps, const KParams& p, int sms, cudaStream_t stream) {
 }
 
 int run(int variant, const void* q, const void* k, const void* v, const float* dq, const float* dk,
-        const float* dv, void* out, int out_dtype, int B, int Hq, int Hkv, int S, int Dqk, int Dv,
-        int causal, float softmax_scale, int flags, int* dev_status, void* stream) {
+        const float* dv, void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S,
+        int Dqk, int Dv, int causal, float softmax_scale, int flags, int* dev_status,
+        void* stream) {
   // ---- argument checks (before anything touches the device)
   if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_BF16) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
@@ -126,8 +127,9 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if ((flags & ATTN_FLAG_TEST_STALL_LOADS) && !dev_status) return ATTN_ERR_INVALID_ARG;
-  if (flags & ~ATTN_FLAG_TEST_STALL_LOADS) return ATTN_ERR_INVALID_ARG;
-  if (causal != 1) return ATTN_ERR_UNSUPPORTED;
+  if (flags & ~(ATTN_FLAG_TEST_STALL_LOADS | ATTN_FLAG_DESCALE_PER_BKV)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (Dv != 128) return ATTN_ERR_UNSUPPORTED;
   if (fp8 ? (Dqk != 128 && Dqk != 192) : (Dqk != 128)) return ATTN_ERR_UNSUPPORTED;
   // index ranges: the kernel's int arithmetic covers B*Hq*ceil(S/256) items
@@ -157,6 +159,9 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   p.status = dev_status;
   p.flags = flags;
   p.wait_limit_ns = (flags & ATTN_FLAG_TEST_STALL_LOADS) ? kTestWaitLimitNs : kWaitLimitNs;
+  p.causal = causal;
+  p.descale_per_bkv = (flags & ATTN_FLAG_DESCALE_PER_BKV) ? 1 : 0;
+  p.lse = lse;
 
   Maps maps;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -197,29 +202,38 @@ extern "C" {
 int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* descale_q,
                  const float* descale_k, const float* descale_v, void* out, int B, int Hq,
                  int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
-  return run(ATTN_VARIANT_LEANP, q, k, v, descale_q, descale_k, descale_v, out, ATTN_OUT_BF16, B,
-             Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+  return run(ATTN_VARIANT_LEANP, q, k, v, descale_q, descale_k, descale_v, out, ATTN_OUT_BF16,
+             nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
 }
 
 int attn_fwd_fp8_exact(const void* q, const void* k, const void* v, const float* descale_q,
                        const float* descale_k, const float* descale_v, void* out, int B,
                        int Hq, int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
   return run(ATTN_VARIANT_EXACT_FP8, q, k, v, descale_q, descale_k, descale_v, out,
-             ATTN_OUT_BF16, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+             ATTN_OUT_BF16, nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
 }
 
 int attn_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                   int S, int Dqk, int Dv, int causal, void* stream) {
-  return run(ATTN_VARIANT_BF16, q, k, v, nullptr, nullptr, nullptr, out, ATTN_OUT_BF16, B, Hq,
-             Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+  return run(ATTN_VARIANT_BF16, q, k, v, nullptr, nullptr, nullptr, out, ATTN_OUT_BF16, nullptr,
+             B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
 }
 
 int attn_fwd_ex(int variant, const void* q, const void* k, const void* v, const float* descale_q,
                 const float* descale_k, const float* descale_v, void* out, int out_dtype, int B,
                 int Hq, int Hkv, int S, int Dqk, int Dv, int causal, float softmax_scale,
                 int flags, int* dev_status, void* stream) {
-  return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, B, Hq, Hkv, S,
-             Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
+  return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, nullptr, B, Hq,
+             Hkv, S, Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
+}
+
+int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
+                  const float* descale_q, const float* descale_k, const float* descale_v,
+                  void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S, int Dqk,
+                  int Dv, int causal, float softmax_scale, int flags, int* dev_status,
+                  void* stream) {
+  return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, lse, B, Hq, Hkv,
+             S, Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
 }
 
 const char* attn_status_string(int status) {

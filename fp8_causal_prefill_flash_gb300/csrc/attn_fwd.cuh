@@ -133,6 +133,9 @@ struct KParams {
   int* status;       // optional device status word
   int flags;
   unsigned long long wait_limit_ns;
+  int causal;          // 1: keys j <= i; 0: all S keys
+  int descale_per_bkv; // descales hold one value per (batch, kv head) instead of one
+  float* lse;          // optional [B, Hq, S] natural-log row sums (nullptr: none)
 };
 
 struct Maps {
@@ -160,7 +163,7 @@ __device__ __forceinline__ void decode_item(const KParams& p, int idx, int& b, i
 // Number of key tiles query tile t of block qb needs (keys < min(S, last row + 1)).
 __device__ __forceinline__ int kv_tiles_for(const KParams& p, int qb, int t) {
   const int need = 2 * qb + t + 1;
-  return need < p.n_kv_tiles ? need : p.n_kv_tiles;
+  return p.causal && need < p.n_kv_tiles ? need : p.n_kv_tiles;
 }
 
 struct __align__(8) Barriers {
@@ -460,15 +463,7 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
   const uint32_t s_col = tmem + lane_base + C::kColS;
   const uint32_t p_col = tmem + lane_base + (t ? C::kColP1 : C::kColP0);
   const uint32_t o_col = tmem + lane_base + (t ? C::kColO1 : C::kColO0);
-  float dqk = 1.0f, dvv = 1.0f;
-  if constexpr (C::kFp8) {
-    dqk = __ldg(p.dq) * __ldg(p.dk);
-    dvv = __ldg(p.dv);
-  }
   const float log2e = 1.4426950408889634f;
-  const float lam = log2e * p.scale * dqk;  // log2 units per unit of s
-  const float lam8 = 8.0f * lam;            // Lean-P code units per unit of s
-  const float lamc = lam8 * (1.0f / 128.0f);
   const LeanPConsts kc = leanp_consts();
   uint32_t s_cnt = 0, o_cnt = 0;
 
@@ -478,6 +473,16 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     int b, h, qb;
     decode_item(p, idx, b, h, qb);
     const int nk = kv_tiles_for(p, qb, t);
+    // descales of this (batch, kv head) and the scale factors they give
+    float dqk = 1.0f, dvv = 1.0f;
+    if constexpr (C::kFp8) {
+      const int di = p.descale_per_bkv ? b * p.Hkv + h / p.group : 0;
+      dqk = __ldg(p.dq + di) * __ldg(p.dk + di);
+      dvv = __ldg(p.dv + di);
+    }
+    const float lam = log2e * p.scale * dqk;  // log2 units per unit of s
+    const float lam8 = 8.0f * lam;            // Lean-P code units per unit of s
+    const float lamc = lam8 * (1.0f / 128.0f);
     const int row = qb * 256 + t * 128 + r;
     float l = 0.0f;    // exact paths: row sum of the unrounded probabilities
     float ref = 0.0f;  // Lean-P: reference binade; exact paths: running max (log2 units)
@@ -503,10 +508,12 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       mbar_arrive(&bars.s_drained[t]);
       if (stamp) FA8_TL(t, j, 2);
       const int key0 = j * kBN;
-      if (key0 + kBN - 1 > row) {  // diagonal tile: mask keys after the row
+      // the last key this row sees: itself (causal) or the last one (S - 1)
+      const int kmax = p.causal ? row : p.S - 1;
+      if (key0 + kBN - 1 > kmax) {  // diagonal or ragged tile: mask the keys beyond
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (key0 + c > row) s[c] = __float_as_uint(-INFINITY);
+          if (key0 + c > kmax) s[c] = __float_as_uint(-INFINITY);
       }
       bool rescale = false;
       float alpha = 1.0f;
@@ -616,6 +623,10 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     tc_fence_after();
     if constexpr (V == kLeanP) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
     const float inv = dvv / l;
+    // log-sum-exp of the row in natural units: the row sum l is relative to
+    // 2^ref (Lean-P: the scaled rounded weights; exact paths: the unrounded p)
+    if (p.lse && row < p.S)
+      p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref + log2f(l)) * 0.6931471805599453f;
     const bool store = row < p.S;
     const size_t orow = ((size_t)b * p.S + (size_t)(row < p.S ? row : 0)) * p.Hq + h;
 #pragma unroll 1

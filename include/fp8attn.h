@@ -13,7 +13,10 @@
  *     out[b, i, h, :] = sum_{j <= i} softmax_j(scale * <q~[b,i,h,:], k~[b,j,g,:]>) v~[b,j,g,:]
  *
  * with g = floor(h * Hkv / Hq) (grouped-query head mapping), q~ = dq * q,
- * k~ = dk * k, v~ = dv * v the dequantized inputs and scale = 1/sqrt(Dqk).
+ * k~ = dk * k, v~ = dv * v the dequantized inputs and scale = 1/sqrt(Dqk)
+ * (attn_fwd_ex / attn_fwd_full take any scale; with causal = 0 the sum runs
+ * over all j < S; with ATTN_FLAG_DESCALE_PER_BKV the descales are per (batch,
+ * kv head)).
  *
  * Three arithmetic paths compute it:
  *   - attn_fwd_fp8: the Lean-P path.  Each probability is an e4m3 code made by
@@ -33,7 +36,7 @@
  * DEVICE memory (per-tensor descales), so a call can be captured in a CUDA
  * graph.  BF16 inputs are bf16 values.
  *
- * Supported: causal = 1, (Dqk, Dv) in {(128, 128), (192, 128)} for FP8 and
+ * Supported: causal = 0 or 1, (Dqk, Dv) in {(128, 128), (192, 128)} for FP8 and
  * (128, 128) for BF16, any S >= 1, B >= 1, Hq % Hkv == 0.  Base addresses must
  * be 16-byte aligned.  The device must be sm_103 (GB300).
  *
@@ -51,13 +54,13 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 2
+#define FP8ATTN_API_VERSION 3
 
 /* Return codes of every entry point. */
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, Hq % Hkv != 0 */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented: causal = 0, other head dims */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid but not implemented: other head dims */
   ATTN_ERR_ARCH = 3,        /* current device is not sm_103 */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map) */
   ATTN_ERR_TIMEOUT = 5      /* a device-side bounded wait expired (see dev_status) */
@@ -80,6 +83,10 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
  * with its tensor memory released.  Requires dev_status != NULL and uses a
  * short (about 0.2 s) wait limit. */
 #define ATTN_FLAG_TEST_STALL_LOADS 1
+/* The three descales hold B*Hkv values each, [B, Hkv] row-major: the Q heads
+ * of kv head g in batch b use entry b*Hkv + g (the per-(batch, kv head)
+ * descales of FP8 flash_attn_func); without the flag, one value each. */
+#define ATTN_FLAG_DESCALE_PER_BKV 2
 
 /*
  * FP8 Lean-P causal prefill attention ("Lean P: one multiply-add instead of an
@@ -87,7 +94,7 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
  *   q, k, v      device pointers to e4m3 bytes in the layouts above
  *   descale_*    device pointers to one fp32 each
  *   out          device pointer, bf16 [B, S, Hq, Dv]
- *   causal       must be 1
+ *   causal       1 (row i sees keys 0 .. i) or 0 (all keys)
  *   stream       cudaStream_t or NULL
  * Returns an attn_status.  A device-side wait expiry cannot be reported here
  * (nothing is read back); use attn_fwd_ex with dev_status to observe it.
@@ -133,6 +140,26 @@ const char* attn_status_string(int status);
 /* Number of kernel launches one call makes (1 for every supported shape;
  * 0 when S == 0 or B == 0 is rejected).  Lets callers count launches. */
 int attn_launches_per_call(void);
+
+/*
+ * The general entry point: attn_fwd_ex plus an optional log-sum-exp output,
+ * for drop-in use behind a flash_attn_func-style interface ("Zyphra ZYFA: FP8
+ * FlashAttention for AMD MI355X", "TL;DR").
+ *   causal     1: row i sees keys 0 .. i; 0: every row sees all S keys
+ *   flags      ATTN_FLAG_DESCALE_PER_BKV for [B, Hkv] descales (FP8 only);
+ *              ATTN_FLAG_TEST_STALL_LOADS as for attn_fwd_ex
+ *   lse        NULL, or a device pointer to fp32 [B, Hq, S] (4-byte aligned):
+ *              lse[b,h,i] = ln sum_j w_ij, the natural log of the row's own
+ *              unnormalised weights (Lean-P: the rounded, scaled weights whose
+ *              sum divides the output; exact paths: exp(z_ij) before rounding),
+ *              z_ij = softmax_scale * descale_q * descale_k * <q_i, k_j>
+ * Other arguments as attn_fwd_ex.  Returns an attn_status.
+ */
+int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
+                  const float* descale_q, const float* descale_k, const float* descale_v,
+                  void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S, int Dqk,
+                  int Dv, int causal, float softmax_scale, int flags, int* dev_status,
+                  void* stream);
 
 /* Input element type for attn_quantize_fp8. */
 typedef enum { ATTN_IN_BF16 = 0, ATTN_IN_F32 = 1 } attn_in_dtype;

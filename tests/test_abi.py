@@ -17,15 +17,15 @@ def lib():
 def test_header_declares_the_entry_points():
     names = fa.declared_functions()
     for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
-              "attn_quantize_fp8", "attn_status_string", "attn_launches_per_call",
-              "attn_api_version"):
+              "attn_quantize_fp8", "attn_fwd_full", "attn_status_string",
+              "attn_launches_per_call", "attn_api_version"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 2
+    assert lib.attn_api_version() == 3
     assert lib.attn_launches_per_call() == 1
 
 
@@ -57,7 +57,8 @@ def call_ex(lib, variant=0, q=P, k=P, v=P, dq=P, dk=P, dv=P, out=P, out_dtype=0,
     (dict(out_dtype=3), fa.ATTN_ERR_INVALID_ARG),
     (dict(flags=1), fa.ATTN_ERR_INVALID_ARG),          # stall test hook needs a status word
     (dict(scale=float("nan")), fa.ATTN_ERR_INVALID_ARG),
-    (dict(causal=0), fa.ATTN_ERR_UNSUPPORTED),
+    (dict(causal=2), fa.ATTN_ERR_INVALID_ARG),
+    (dict(flags=8), fa.ATTN_ERR_INVALID_ARG),          # unknown flag
     (dict(Dqk=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(Dv=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(variant=2, Dqk=192), fa.ATTN_ERR_UNSUPPORTED),
@@ -67,15 +68,16 @@ def test_bad_arguments_are_rejected_before_launch(lib, kw, want):
 
 
 def test_bf16_needs_no_descales(lib):
-    # descales may be NULL on the BF16 path; with causal = 0 the call stops at
+    # descales may be NULL on the BF16 path; with Dqk = 192 the call stops at
     # the (host-side) support check, before any device work
-    assert call_ex(lib, variant=2, dq=None, dk=None, dv=None, causal=0) == fa.ATTN_ERR_UNSUPPORTED
+    assert call_ex(lib, variant=2, dq=None, dk=None, dv=None, causal=0, Dqk=192) == \
+        fa.ATTN_ERR_UNSUPPORTED
 
 
 def test_product_entry_points_check_arguments(lib):
     assert lib.attn_fwd_fp8(None, P, P, P, P, P, P, 1, 2, 2, 128, 128, 128, 1, None) == \
         fa.ATTN_ERR_INVALID_ARG
-    assert lib.attn_fwd_fp8_exact(P, P, P, P, P, P, P, 1, 2, 2, 128, 128, 128, 0, None) == \
+    assert lib.attn_fwd_fp8_exact(P, P, P, P, P, P, P, 1, 2, 2, 128, 128, 64, 0, None) == \
         fa.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd_bf16(P, P, P, P, 1, 2, 2, 128, 192, 128, 1, None) == \
         fa.ATTN_ERR_UNSUPPORTED
@@ -94,3 +96,15 @@ def test_quantize_argument_errors(lib):
     assert q(vp(0x10008), 0, P, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG  # x needs 16 B
     assert q(P, 0, vp(0x10004), P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG  # codes 16 B
     assert q(P, 0, MIS, P, 1, 1, 1, 128, 0, None) == fa.ATTN_ERR_INVALID_ARG    # codes alignment
+
+
+def test_full_entry_point_checks_arguments(lib):
+    """attn_fwd_full validates the LSE pointer and the descale flag like the rest."""
+    f = lib.attn_fwd_full
+    args = lambda **kw: [kw.get("variant", 0), P, P, P, P, P, P, P, 0, kw.get("lse", None), 1, 2, 2,
+                         128, 128, kw.get("Dv", 128), kw.get("causal", 1), 0.0, kw.get("flags", 0),
+                         None, None]
+    assert f(*args(lse=MIS)) == fa.ATTN_ERR_INVALID_ARG                  # misaligned lse
+    assert f(*args(flags=4)) == fa.ATTN_ERR_INVALID_ARG                  # unknown flag
+    assert f(*args(causal=-1)) == fa.ATTN_ERR_INVALID_ARG
+    assert f(*args(Dv=64, flags=fa.ATTN_FLAG_DESCALE_PER_BKV)) == fa.ATTN_ERR_UNSUPPORTED

@@ -193,8 +193,9 @@ def test_stalled_loads_report_timeout_and_context_survives():
 def test_argument_errors_are_reported():
     case = wl.fp8_gaussian_case(1, 2, 2, 64, 128, 128)
     q, k, v, d = dev_fp8(case)
-    _, st = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d, causal=False, raise_on_error=False)
-    assert st == fa.ATTN_ERR_UNSUPPORTED
+    v64 = torch.zeros((1, 64, 2, 64), dtype=torch.uint8, device="cuda")
+    _, st = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v64, *d, raise_on_error=False)
+    assert st == fa.ATTN_ERR_UNSUPPORTED  # Dv = 64
     q3 = torch.zeros((1, 64, 3, 128), dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd_fp8(q3, k, v, *d)
