@@ -90,7 +90,11 @@ def _load():
         lib.oracle_emul_exact_ex.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, dp, ctypes.c_int,
                                              ctypes.c_int, *shape, ctypes.c_double, i64p,
                                              ctypes.c_int64, ctypes.c_double, dp, dp, dp]
-        for fn in ("oracle_ref_fp64_ex", "oracle_emul_leanp_ex", "oracle_emul_exact_ex"):
+        lib.oracle_emul_variant_e.argtypes = [vp, vp, vp, dp, dp, dp, ctypes.c_int, ctypes.c_int,
+                                              *shape, ctypes.c_double, i64p, ctypes.c_int64, dp,
+                                              dp]
+        for fn in ("oracle_ref_fp64_ex", "oracle_emul_leanp_ex", "oracle_emul_exact_ex",
+                   "oracle_emul_variant_e"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.oracle_quantize_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -328,7 +332,9 @@ def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, caus
               kappa=DEFAULT_KAPPA):
     """All definitions with every option (non-causal, per-(batch, kv head)
     descales) and the per-row log-sum-exp.  ``path`` is "ref" (fp64 on e4m3
-    codes), "ref_bf16", "leanp", "exact_fp8" or "bf16".  Returns ``(out, amb,
+    codes), "ref_bf16", "leanp", "exact_fp8", "bf16" or "variant_e" (the
+    diagnostic: Lean-P's blocks and rounded sum with exact, RNE-rounded
+    weights; no GPU counterpart).  Returns ``(out, amb,
     lse)``: out [B,S,Hq,Dv] or (n, Dv) for ``rows``; amb per row (None for the
     reference and BF16 paths); lse per row, natural log of the row sum (the
     unnormalised weights of that path), shaped [B,Hq,S] or (n,)."""
@@ -351,6 +357,9 @@ def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, caus
     elif path == "leanp":
         rc = lib.oracle_emul_leanp_ex(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
                                       _dptr(amb), _dptr(lse))
+    elif path == "variant_e":
+        amb = None
+        rc = lib.oracle_emul_variant_e(_ptr(q), _ptr(k), _ptr(v), *args, _dptr(out), _dptr(lse))
     elif path in ("exact_fp8", "bf16"):
         rc = lib.oracle_emul_exact_ex(_ptr(q), _ptr(k), _ptr(v), int(bf16), *args, float(kappa),
                                       _dptr(out), None if amb is None else _dptr(amb), _dptr(lse))

@@ -308,9 +308,13 @@ static int leanp_code(double x) {
   return (int)f;
 }
 
+/* exact_p = 1 gives the diagnostic variant E: the same blocks, exponents and
+ * rounded row sum, but each weight is the exact value 2^(u_j/8 - e + T)
+ * rounded to e4m3 (nearest even) instead of the Lean-P code, so that E - A
+ * measures the block scale and the rounded sum and Lean-P - E the code. */
 static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts_t o, shape_t sh,
                       double scale, const int64_t *rows, int64_t nrows, double kappa, double *out,
-                      double *amb, double *lse) {
+                      double *amb, double *lse, int exact_p) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
@@ -348,6 +352,11 @@ static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts
       double f = ldexp(1.0, eb[bb] - E - LEANP_T);
       for (int j = j0; j < j1; ++j) {
         double x = u[j] - 8.0 * eb[bb] + LEANP_C;
+        if (exact_p) {
+          w[j] = oracle_e4m3_round(exp2(u[j] / 8.0 - eb[bb] + LEANP_T)) * f;
+          L += w[j];
+          continue;
+        }
         int c = leanp_code(x);
         w[j] = oracle_e4m3_decode((unsigned)c) * f;
         L += w[j];
@@ -398,7 +407,7 @@ int oracle_emul_leanp(const uint8_t *q, const uint8_t *k, const uint8_t *v, doub
                       double *amb) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
   opts_t o = {&dq, &dk, &dv, 0, 1};
-  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, NULL);
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, NULL, 0);
 }
 
 int oracle_emul_leanp_ex(const uint8_t *q, const uint8_t *k, const uint8_t *v, const double *dq,
@@ -409,7 +418,18 @@ int oracle_emul_leanp_ex(const uint8_t *q, const uint8_t *k, const uint8_t *v, c
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
   if (!dq || !dk || !dv) return ORACLE_BAD_ARG;
   opts_t o = {dq, dk, dv, per_bkv, causal};
-  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse);
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse, 0);
+}
+
+/* Diagnostic variant E (no GPU counterpart): see leanp_impl.  amb unused. */
+int oracle_emul_variant_e(const uint8_t *q, const uint8_t *k, const uint8_t *v, const double *dq,
+                          const double *dk, const double *dv, int per_bkv, int causal, int B,
+                          int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
+                          const int64_t *rows, int64_t nrows, double *out, double *lse) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  if (!dq || !dk || !dv) return ORACLE_BAD_ARG;
+  opts_t o = {dq, dk, dv, per_bkv, causal};
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, 0.0, out, NULL, lse, 1);
 }
 
 /* ---------------------------------------------------------------------------

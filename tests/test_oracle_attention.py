@@ -389,3 +389,26 @@ def test_bf16_reference_noncausal_matches_sdpa(oracle_mod):
     q, k, v = (oracle_mod.bf16_decode(a) for a in (b.q, b.k, b.v))
     want, want_lse = _sdpa(q, k, v, False, 1.0 / math.sqrt(64))
     assert np.max(np.abs(out - want)) < 1e-12 and np.max(np.abs(lse - want_lse)) < 1e-12
+
+
+def test_variant_e_isolates_the_code(oracle_mod):
+    """Variant E keeps Lean-P's blocks, exponents and rounded row sum but rounds
+    the exact weight to nearest e4m3: with V = 1 it is exactly 1 like Lean-P
+    (rounded sum), its weights sit within half an e4m3 ulp of the exact ones,
+    and where every logit is an integer number of binades (exact codes) it
+    equals Lean-P."""
+    c = wl.fp8_gaussian_case(1, 2, 2, 200, 128, 128, seeds=(121, 122, 123))
+    ones = np.full_like(c.v, 0x38)
+    e1, _, _ = oracle_mod.attention("variant_e", c.q, c.k, ones, c.dq, c.dk, 1.0)
+    assert np.max(np.abs(e1 - 1.0)) < 1e-12
+    _, _, ref = oracle_mod.attention("ref", c.q, c.k, c.v, c.dq, c.dk, c.dv)
+    _, _, le = oracle_mod.attention("variant_e", c.q, c.k, c.v, c.dq, c.dk, c.dv)
+    assert np.max(np.abs(le - ref)) < math.log(1.0 + 2.0 ** -4)
+    # logits on integer binades: q = 1, k in {0, 1, 2, ...}, scale = ln 2
+    S = 64
+    q = codes_of(np.ones((1, S, 1, 1), np.float32))
+    k = codes_of(np.arange(S, dtype=np.float32).reshape(1, S, 1, 1) % 8)
+    v = codes_of(np.linspace(-2, 2, S).astype(np.float32).round(0).reshape(1, S, 1, 1))
+    a, _, _ = oracle_mod.attention("variant_e", q, k, v, scale=LN2)
+    b, _, _ = oracle_mod.attention("leanp", q, k, v, scale=LN2)
+    assert np.array_equal(a, b)
