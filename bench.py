@@ -70,8 +70,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3990294016,
-                    "sources_sha256": "8bc1b03cac4c06c8634160d07b6c604a6111abdfc1b28b6e0629e3f50bb15b07"}
+PROFILED_TRAFFIC = {"bytes": 3935891712,
+                    "sources_sha256": "ecfcace81167e0c3098af3fd1ba6cfa0c9dd2e6f1cf8744704731b858307f21b"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")
