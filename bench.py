@@ -428,7 +428,11 @@ def run_sweep(args):
             q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
             d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
             paths = {"leanp": lambda: fa.attn_fwd_fp8(q, k, v, *d, out=out),
-                     "exact_fp8_ablation": lambda: fa.attn_fwd_fp8_exact(q, k, v, *d, out=out)}
+                     "exact_fp8_ablation": lambda: fa.attn_fwd_fp8_exact(q, k, v, *d, out=out),
+                     # Lean-P's block scale and rounded sum, exponential for the code
+                     "block_exact": lambda: fa.attn_fwd_ex(fa.ATTN_VARIANT_BLOCK_EXACT, q, k, v,
+                                                           *d, out=out,
+                                                           out_dtype=fa.ATTN_OUT_BF16)}
             peak = peaks["bf16_burst"] * FP8_OVER_BF16
             in_bytes = (case.q.nbytes + case.k.nbytes + case.v.nbytes)
         else:

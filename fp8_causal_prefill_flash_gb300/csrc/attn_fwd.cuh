@@ -39,6 +39,10 @@
 //              row sum").
 //   kExactFp8  p = 2^(x - m) on the MUFU, rounded to e4m3, unrounded row sum.
 //   kBf16      as kExactFp8 with bf16 operands and probabilities.
+//   kBlockExact  diagnostic: the block exponents, UE8M0 factors and rounded
+//              row sum of kLeanP, but each probability is 2^(x/8 - e + T) from
+//              the MUFU rounded to the nearest e4m3 instead of the Lean-P
+//              code, so that it differs from kLeanP in the code step alone.
 #pragma once
 
 #include <cstdint>
@@ -64,7 +68,7 @@ __device__ unsigned long long fa8_timeline[4][64][8];
   } while (0)
 #endif
 
-enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2 };
+enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2, kBlockExact = 3 };
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per K/V tile
@@ -86,6 +90,8 @@ constexpr float kLazyBinades = 8.0f;
 template <int V, int DQK>
 struct Cfg {
   static constexpr bool kFp8 = V != kBf16;
+  // per-64-key power-of-two block scale and the rounded row sum (O column 128)
+  static constexpr bool kBlockScaled = V == kLeanP || V == kBlockExact;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = DQK * kElem;             // bytes of one Q/K row
   static constexpr int kFullPanels = kRowBytes / 128;       // 128-byte swizzled panels
@@ -101,14 +107,14 @@ struct Cfg {
   static constexpr int kSmemV = kSmemK + kStages * kQkTileBytes;
   // Lean-P: 128 keys x 128 bytes of e4m3 1.0, the second N-atom of the P.V
   // B operand, so that O's column 128 accumulates the rounded row sum
-  static constexpr int kOnesBytes = V == kLeanP ? 128 * 128 : 0;
+  static constexpr int kOnesBytes = kBlockScaled ? 128 * 128 : 0;
   static constexpr int kSmemOnes = kSmemV + kStages * kVTileBytes;
   static constexpr int kSmemBytes = kSmemOnes + kOnesBytes;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kQkSteps = kRowBytes / 32;       // one MMA per 32 bytes of K
   static constexpr int kPvSteps = kFp8 ? 4 : 8;         // 128 keys / (32 fp8 or 16 bf16)
   static constexpr int kPCols = kFp8 ? 32 : 64;         // TMEM columns of P per tile
-  static constexpr int kPvN = V == kLeanP ? 144 : 128;  // P.V N (with the ones column)
+  static constexpr int kPvN = kBlockScaled ? 144 : 128;  // P.V N (with the ones column)
   // tensor-memory columns
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColP0 = 128, kColP1 = kFp8 ? 176 : 192;
@@ -519,7 +525,7 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       float alpha = 1.0f;
       uint32_t pw[C::kPCols];
       uint32_t sfa = 0x7F7F7F7Fu;
-      if constexpr (V == kLeanP) {
+      if constexpr (C::kBlockScaled) {
         const float m0 = block_max64(s, 0), m1 = block_max64(s, 64);
         // block exponents e = ceil(lam*max): the block maximum lands in (2^(T-1), 2^T]
         const float e0 = ceilf(m0 * lam8 * 0.125f), e1 = ceilf(m1 * lam8 * 0.125f);
@@ -541,11 +547,24 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         // -inf scores, which give code 0 whatever the bias
         const float b0 = v0 ? (kLeanC - 8.0f * e0) * (1.0f / 128.0f) : 0.0f;
         const float b1 = v1 ? (kLeanC - 8.0f * e1) * (1.0f / 128.0f) : 0.0f;
+        if constexpr (V == kLeanP) {
 #pragma unroll
-        for (int w = 0; w < 32; ++w)
-          pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
-                               __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
-                               lamc, w < 16 ? b0 : b1, kc);
+          for (int w = 0; w < 32; ++w)
+            pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
+                                 __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
+                                 lamc, w < 16 ? b0 : b1, kc);
+        } else {
+          // exponent x/8 - e + T = s*lam + (T - e); masked keys (-inf) give 0
+          const float g0 = v0 ? (float)kLeanT - e0 : 0.0f, g1 = v1 ? (float)kLeanT - e1 : 0.0f;
+#pragma unroll
+          for (int w = 0; w < 32; ++w) {
+            const float g = w < 16 ? g0 : g1;
+            float pv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, g));
+            pw[w] = f32x2_to_e4m3x2(pv[0], pv[1]) | (f32x2_to_e4m3x2(pv[2], pv[3]) << 16);
+          }
+        }
         // scale factor bytes: K-steps 0-1 (block 0) and 2-3 (block 1)
         sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
       } else {
@@ -600,7 +619,7 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(o_col + c, o);
         }
-        if constexpr (V == kLeanP) {  // the row-sum column
+        if constexpr (C::kBlockScaled) {  // the row-sum column
           const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
           tmem_st1(o_col + 128, __float_as_uint(lv));
         }
@@ -621,7 +640,7 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     // epilogue: out = dv * O / l
     if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
     tc_fence_after();
-    if constexpr (V == kLeanP) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
+    if constexpr (C::kBlockScaled) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
     const float inv = dvv / l;
     // log-sum-exp of the row in natural units: the row sum l is relative to
     // 2^ref (Lean-P: the scaled rounded weights; exact paths: the unrounded p)

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 3
+#define FP8ATTN_API_VERSION 4
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -70,7 +70,15 @@ typedef enum {
 typedef enum {
   ATTN_VARIANT_LEANP = 0,     /* FP8 Lean-P (attn_fwd_fp8) */
   ATTN_VARIANT_EXACT_FP8 = 1, /* FP8 exact-softmax ablation (attn_fwd_fp8_exact) */
-  ATTN_VARIANT_BF16 = 2       /* BF16 exact softmax (attn_fwd_bf16) */
+  ATTN_VARIANT_BF16 = 2,      /* BF16 exact softmax (attn_fwd_bf16) */
+  /* FP8 diagnostic: Lean-P's 64-key power-of-two block scale and rounded row
+   * sum, with each probability 2^(x/8 - e + T) taken from the exponential
+   * unit and rounded to the nearest e4m3 instead of the Lean-P code.  It
+   * differs from ATTN_VARIANT_LEANP in the code step alone, which isolates
+   * what the one-multiply-add code costs in accuracy and saves in time
+   * ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X", "Lean P" and
+   * "Per-block scaling and a rounded row sum"). */
+  ATTN_VARIANT_BLOCK_EXACT = 3
 } attn_variant;
 
 /* Output element type for attn_fwd_ex. */

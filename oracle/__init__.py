@@ -91,8 +91,8 @@ def _load():
                                              ctypes.c_int, *shape, ctypes.c_double, i64p,
                                              ctypes.c_int64, ctypes.c_double, dp, dp, dp]
         lib.oracle_emul_variant_e.argtypes = [vp, vp, vp, dp, dp, dp, ctypes.c_int, ctypes.c_int,
-                                              *shape, ctypes.c_double, i64p, ctypes.c_int64, dp,
-                                              dp]
+                                              *shape, ctypes.c_double, i64p, ctypes.c_int64,
+                                              ctypes.c_double, dp, dp, dp]
         for fn in ("oracle_ref_fp64_ex", "oracle_emul_leanp_ex", "oracle_emul_exact_ex",
                    "oracle_emul_variant_e"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -334,7 +334,7 @@ def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, caus
     descales) and the per-row log-sum-exp.  ``path`` is "ref" (fp64 on e4m3
     codes), "ref_bf16", "leanp", "exact_fp8", "bf16" or "variant_e" (the
     diagnostic: Lean-P's blocks and rounded sum with exact, RNE-rounded
-    weights; no GPU counterpart).  Returns ``(out, amb,
+    weights, the GPU's ATTN_VARIANT_BLOCK_EXACT).  Returns ``(out, amb,
     lse)``: out [B,S,Hq,Dv] or (n, Dv) for ``rows``; amb per row (None for the
     reference and BF16 paths); lse per row, natural log of the row sum (the
     unnormalised weights of that path), shaped [B,Hq,S] or (n,)."""
@@ -358,8 +358,8 @@ def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, caus
         rc = lib.oracle_emul_leanp_ex(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
                                       _dptr(amb), _dptr(lse))
     elif path == "variant_e":
-        amb = None
-        rc = lib.oracle_emul_variant_e(_ptr(q), _ptr(k), _ptr(v), *args, _dptr(out), _dptr(lse))
+        rc = lib.oracle_emul_variant_e(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
+                                       _dptr(amb), _dptr(lse))
     elif path in ("exact_fp8", "bf16"):
         rc = lib.oracle_emul_exact_ex(_ptr(q), _ptr(k), _ptr(v), int(bf16), *args, float(kappa),
                                       _dptr(out), None if amb is None else _dptr(amb), _dptr(lse))

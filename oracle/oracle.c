@@ -353,8 +353,16 @@ static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts
       for (int j = j0; j < j1; ++j) {
         double x = u[j] - 8.0 * eb[bb] + LEANP_C;
         if (exact_p) {
-          w[j] = oracle_e4m3_round(exp2(u[j] / 8.0 - eb[bb] + LEANP_T)) * f;
+          double y = exp2(u[j] / 8.0 - eb[bb] + LEANP_T);
+          w[j] = oracle_e4m3_round(y) * f;
           L += w[j];
+          if (amb) {
+            /* the nearest e4m3 may flip when y moves by the relative error of
+             * its fp32 argument (du/8 binades) and of a 2^-20-accurate 2^x */
+            double d = log(2.0) * du[j] / 8.0 + ldexp(1.0, -20);
+            double lo = oracle_e4m3_round(y * (1.0 - d)), hi = oracle_e4m3_round(y * (1.0 + d));
+            dmass += (hi - lo) * f;
+          }
           continue;
         }
         int c = leanp_code(x);
@@ -378,8 +386,14 @@ static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts
           int ea = (int)nt, eb2 = (int)nt + 1; /* ceil is nt or nt+1 */
           double fa = ldexp(1.0, ea - E - LEANP_T), fb = ldexp(1.0, eb2 - E - LEANP_T);
           for (int j = j0; j < j1; ++j) {
-            double wa = oracle_e4m3_decode((unsigned)leanp_code(u[j] - 8.0 * ea + LEANP_C)) * fa;
-            double wb = oracle_e4m3_decode((unsigned)leanp_code(u[j] - 8.0 * eb2 + LEANP_C)) * fb;
+            double wa, wb;
+            if (exact_p) {
+              wa = oracle_e4m3_round(exp2(u[j] / 8.0 - ea + LEANP_T)) * fa;
+              wb = oracle_e4m3_round(exp2(u[j] / 8.0 - eb2 + LEANP_T)) * fb;
+            } else {
+              wa = oracle_e4m3_decode((unsigned)leanp_code(u[j] - 8.0 * ea + LEANP_C)) * fa;
+              wb = oracle_e4m3_decode((unsigned)leanp_code(u[j] - 8.0 * eb2 + LEANP_C)) * fb;
+            }
             dmass += fabs(wa - wb);
           }
         }
@@ -421,15 +435,17 @@ int oracle_emul_leanp_ex(const uint8_t *q, const uint8_t *k, const uint8_t *v, c
   return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse, 0);
 }
 
-/* Diagnostic variant E (no GPU counterpart): see leanp_impl.  amb unused. */
+/* Diagnostic variant E: see leanp_impl.  amb as for Lean-P (kappa: the
+ * relative bound of the fp32 dot product, as in oracle_emul_leanp). */
 int oracle_emul_variant_e(const uint8_t *q, const uint8_t *k, const uint8_t *v, const double *dq,
                           const double *dk, const double *dv, int per_bkv, int causal, int B,
                           int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
-                          const int64_t *rows, int64_t nrows, double *out, double *lse) {
+                          const int64_t *rows, int64_t nrows, double kappa, double *out,
+                          double *amb, double *lse) {
   shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
   if (!dq || !dk || !dv) return ORACLE_BAD_ARG;
   opts_t o = {dq, dk, dv, per_bkv, causal};
-  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, 0.0, out, NULL, lse, 1);
+  return leanp_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse, 1);
 }
 
 /* ---------------------------------------------------------------------------

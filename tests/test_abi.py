@@ -25,7 +25,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 3
+    assert lib.attn_api_version() == 4
     assert lib.attn_launches_per_call() == 1
 
 
@@ -54,6 +54,9 @@ def call_ex(lib, variant=0, q=P, k=P, v=P, dq=P, dk=P, dv=P, out=P, out_dtype=0,
     (dict(S=0), fa.ATTN_ERR_INVALID_ARG),
     (dict(B=0), fa.ATTN_ERR_INVALID_ARG),
     (dict(variant=7), fa.ATTN_ERR_INVALID_ARG),
+    (dict(variant=4), fa.ATTN_ERR_INVALID_ARG),
+    (dict(variant=3, dq=None), fa.ATTN_ERR_INVALID_ARG),       # block-exact is an FP8 path
+    (dict(variant=3, Dv=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(out_dtype=3), fa.ATTN_ERR_INVALID_ARG),
     (dict(flags=1), fa.ATTN_ERR_INVALID_ARG),          # stall test hook needs a status word
     (dict(scale=float("nan")), fa.ATTN_ERR_INVALID_ARG),
