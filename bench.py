@@ -70,8 +70,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3935891712,
-                    "sources_sha256": "ecfcace81167e0c3098af3fd1ba6cfa0c9dd2e6f1cf8744704731b858307f21b"}
+PROFILED_TRAFFIC = {"bytes": 3933796608,
+                    "sources_sha256": "9e5f7c13574bf631339196c5000513c63e2a4c0ef6cb74ffb55a5bdab207d67b"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")
@@ -385,12 +385,14 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    h_warm = output_sha256(out)
     clocks.start()
     time.sleep(0.3)
     e_start = meter.read_mj()
     ms = timed(step, args.steps, 0)
     e_end = meter.read_mj()
     clk = clocks.stop()
+    h_timed = output_sha256(out)
     if args.leanp_only:
         if rank == 0:
             print(json.dumps({"workload": workload, "S": S, "ms_per_step": ms,
@@ -452,6 +454,8 @@ def run_ours(args, rank, world, local_rank):
                     "serial": {"value": job_tflops(F, world, ms_e2e_serial),
                                "ms_per_step": ms_e2e_serial}},
             "gpu_launches": args.steps,
+            "determinism": {"output_sha256": h_timed, "same_after_warmup_and_timed_steps":
+                            h_warm == h_timed},
             "clocks": clk,
             "energy": energy_report(e_start, e_end, F * args.steps)}
 
@@ -463,7 +467,7 @@ def run_ours(args, rank, world, local_rank):
         emu, dt = oracle_leg(case, rows)
         line["cpu_baseline"] = {
             "value": rows_flops(rows, Dqk, Dv) / dt / 1e12, "unit": "TFLOP/s",
-            "cores": cores_used(), "kind": "oracle",
+            "cores": cores_used(), "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{len(rows)} random (head, row) pairs of {workload}, oracle_emul_leanp, "
                       f"{dt:.1f} s"}
         acc_rows = rows[: args.acc_rows]
@@ -479,6 +483,125 @@ def run_ours(args, rank, world, local_rank):
             "leanp_max_abs_vs_emulation": float(np.max(np.abs(pick(o_lp, rows) - emu)))}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    return 0
+
+
+# --only PATH: the workload each path is profiled on (headline FP8 shape, the
+# BF16 configuration for the BF16 path)
+ONLY_PATHS = {"leanp": "fp8_h32_s32k_d128", "exact_fp8": "fp8_h32_s32k_d128",
+              "block_exact": "fp8_h32_s32k_d128", "bf16": "bf16_gqa_h32_8_s16k_d128"}
+
+
+def run_only(args):
+    """Warm-up and timed launches of one kernel alone (for ncu captures)."""
+    import torch
+
+    import fp8_causal_prefill_flash_gb300 as fa
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+    fa.build()
+    fa.load_library()
+    dev = torch.device("cuda", 0)
+    name = ONLY_PATHS[args.only]
+    case = wl.make_case(name, S=args.S)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+    if args.only == "bf16":
+        q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                   for a in (case.q, case.k, case.v))
+        fn = lambda: fa.attn_fwd_bf16(q, k, v, out=out)
+    else:
+        q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+        d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+        variant = {"leanp": fa.ATTN_VARIANT_LEANP, "exact_fp8": fa.ATTN_VARIANT_EXACT_FP8,
+                   "block_exact": fa.ATTN_VARIANT_BLOCK_EXACT}[args.only]
+        fn = lambda: fa.attn_fwd_ex(variant, q, k, v, *d, out=out, out_dtype=fa.ATTN_OUT_BF16)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"path": args.only, "workload": name, "S": S, "ms_per_step": ms,
+                      "tflops_causal": causal_flops(B, Hq, S, Dqk, Dv) / (ms * 1e-3) / 1e12}),
+          flush=True)
+    return 0
+
+
+def output_sha256(t):
+    """SHA-256 of a device tensor's bytes (the determinism check)."""
+    import hashlib
+
+    import torch
+    return hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes()).hexdigest()
+
+
+def cpu_model():
+    """The host CPU's model name as lscpu reports it (else the platform's)."""
+    try:
+        txt = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in txt.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+_CPU_ONE_CORE = """
+import json, sys, time
+sys.path.insert(0, {root!r})
+import oracle
+from fp8_causal_prefill_flash_gb300 import workloads as wl
+c = wl.make_case("fp8_h2_s256_d128")
+oracle.build()
+res = {{}}
+for name, fn in (("ref_fp64", oracle.ref_fp64), ("emul_leanp", lambda *a: oracle.emul_leanp(*a)[0])):
+    t0 = time.perf_counter()
+    fn(c.q, c.k, c.v, c.dq, c.dk, c.dv)
+    res[name] = time.perf_counter() - t0
+print(json.dumps(res))
+"""
+
+
+def run_cpu_sweep(args):
+    """The oracle on the host cores: every configuration on a bounded sample
+    of rows (the pass the GPU computes, ref_fp64 and emul_leanp), and C1 in
+    full on one core (a child process with OMP_NUM_THREADS=1)."""
+    from fp8_causal_prefill_flash_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    model, cores = cpu_model(), cores_used()
+    for name, cfg in wl.CONFIGS.items():
+        if not cfg["kind"].startswith("fp8"):
+            continue
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        n = min(args.cpu_rows, B * Hq * S)
+        rows = sample_rows(S, Hq, n, 7)
+        res = {}
+        for leg, fn in (("ref_fp64", lambda: oracle.ref_fp64(case.q, case.k, case.v, case.dq,
+                                                             case.dk, case.dv, rows=rows)),
+                        ("emul_leanp", lambda: oracle.emul_leanp(case.q, case.k, case.v, case.dq,
+                                                                 case.dk, case.dv, rows=rows))):
+            t0 = time.perf_counter()
+            fn()
+            dt = time.perf_counter() - t0
+            res[leg] = {"s": dt, "gflops": rows_flops(rows, Dqk, Dv) / dt / 1e9}
+        print(json.dumps({"workload": name, "rows": int(n), "cores": cores, "cpu_model": model,
+                          **res}), flush=True)
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    root = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-c", _CPU_ONE_CORE.format(root=root)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    one = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-300:]}
+    print(json.dumps({"workload": "fp8_h2_s256_d128", "rows": "all", "cores": 1,
+                      "cpu_model": model, "seconds": one}), flush=True)
     return 0
 
 
@@ -523,15 +646,17 @@ def run_sweep(args):
                 fn()
             torch.cuda.synchronize()
             n = args.steps
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(n):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+            ev[0].record()
+            for i in range(n):
                 fn()
-            e1.record()
+                ev[i + 1].record()
             torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / n
+            per = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+            ms = ev[0].elapsed_time(ev[n]) / n
             tf = F / (ms * 1e-3) / 1e12
             print(json.dumps({"workload": name, "path": path, "ms": ms, "tflops_causal": tf,
+                              "ms_median": statistics.median(per), "ms_min": min(per),
                               "tflops_square_formula": 2 * tf, "peak": peak,
                               "frac_of_peak": tf / peak, "hbm_gbs": io_bytes / (ms * 1e-3) / 1e9,
                               "peak_source": peaks["source"], "iterations": n}), flush=True)
@@ -672,6 +797,11 @@ def main():
     ap.add_argument("--S", type=int, default=None, help="override the sequence length (profiling)")
     ap.add_argument("--leanp-only", action="store_true",
                     help="time only the Lean-P kernel and print a short line (profiling)")
+    ap.add_argument("--only", choices=list(ONLY_PATHS), default=None,
+                    help="time one kernel alone on its workload (profiling)")
+    ap.add_argument("--cpu-sweep", action="store_true",
+                    help="time the oracle on every configuration (bounded samples) and C1 "
+                         "in full on one core")
     ap.add_argument("--sweep", action="store_true",
                     help="time every path on every configuration, one JSON line each")
     ap.add_argument("--clock-study", action="store_true",
@@ -689,6 +819,10 @@ def main():
         return run_reference(args, rank, world)
     if args.sweep:
         return run_sweep(args)
+    if args.only:
+        return run_only(args)
+    if args.cpu_sweep:
+        return run_cpu_sweep(args)
     if args.clock_study:
         return run_clock_study(args)
     if world > 1:
