@@ -31,7 +31,7 @@
  *   "TL;DR" names that interface): causal or not, descales per (batch, kv
  *   head) or per tensor, and a per-row log-sum-exp of the path's own row sum.
  *
- * Readings where the articles are silent (each is listed in the design doc):
+ * Readings where the articles are silent or ambiguous:
  *   - e4m3 is OCP E4M3 (bias 7, max 448, S.1111.111 = NaN, no infinities).
  *   - scale = softmax_scale argument (1/sqrt(Dqk) by default), per-tensor fp32
  *     descales, query head h reads kv head floor(h*Hkv/Hq).
