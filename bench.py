@@ -50,6 +50,16 @@ def rows_flops(rows, Dqk, Dv):
     return float(sum(2.0 * (Dqk + Dv) * (int(i) + 1) for _, _, i in rows))
 
 
+# The articles' own figure for this metric and workload: 2672 TFLOP/s for
+# FP8 Lean-P at head dim 128, S = 32K, Gaussian inputs ("Zyphra ZYFA: FP8
+# FlashAttention for AMD MI355X", "How fast is ZYFA?").  It was measured on an
+# AMD MI355X, so the ratio is context, not a target.  The articles give 53% of
+# that GPU's dense FP8 peak for it, which fits the causal FLOP count used here.
+PAGES_TFLOPS = 2672.0
+PAGES_NOTE = ("value / 2672 TFLOP/s, the articles' figure for FP8 Lean-P at hd128, S=32K on "
+              "AMD MI355X (other hardware; causal FLOP count)")
+
+
 def max_over_ranks(ms, device=None):
     """Largest per-rank step time (the job is as slow as its slowest rank)."""
     import torch
@@ -317,7 +327,8 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": tflops / PAGES_TFLOPS,
+            "vs_baseline_note": PAGES_NOTE, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "Dqk": Dqk,
                        "Dv": Dv, "sample_rows_per_step": n_rows},
             "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(),
@@ -432,7 +443,8 @@ def run_ours(args, rank, world, local_rank):
     per_gpu = F / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": job_tflops(F, world, ms), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": job_tflops(F, world, ms) / PAGES_TFLOPS, "vs_baseline_note": PAGES_NOTE,
             "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
             "config": {"workload": workload, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "Dqk": Dqk,
                        "Dv": Dv, "inputs": "N(0,1) per-tensor e4m3, seeds 30/31/32",
