@@ -501,7 +501,9 @@ def run_ours(args, rank, world, local_rank):
 # --only PATH: the workload each path is profiled on (headline FP8 shape, the
 # BF16 configuration for the BF16 path)
 ONLY_PATHS = {"leanp": "fp8_h32_s32k_d128", "exact_fp8": "fp8_h32_s32k_d128",
-              "block_exact": "fp8_h32_s32k_d128", "bf16": "bf16_gqa_h32_8_s16k_d128"}
+              "block_exact": "fp8_h32_s32k_d128", "bf16": "bf16_gqa_h32_8_s16k_d128",
+              "quantize": "quantize_bf16_s32k_h32_d128",
+              "quantize_hadamard": "quantize_bf16_s32k_h32_d128"}
 
 
 def run_only(args):
@@ -515,6 +517,28 @@ def run_only(args):
     fa.load_library()
     dev = torch.device("cuda", 0)
     name = ONLY_PATHS[args.only]
+    if args.only.startswith("quantize"):
+        # a bf16 tensor of the headline Q shape (seeded), quantised per tensor
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(60)
+        x = torch.randn((1, args.S or 32768, 32, 128), generator=gen, device=dev).to(torch.bfloat16)
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+        ds = torch.empty(1, dtype=torch.float32, device=dev)
+        rot = args.only == "quantize_hadamard"
+        fn = lambda: fa.attn_quantize_fp8(x, hadamard=rot, codes=codes, descale=ds)
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        print(json.dumps({"path": args.only, "workload": name, "ms_per_step": ms,
+                          "gbs_moved": x.numel() * 5 / (ms * 1e-3) / 1e9}), flush=True)
+        return 0
     case = wl.make_case(name, S=args.S)
     B, Hq, Hkv, S, Dqk, Dv = case.shape
     out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)

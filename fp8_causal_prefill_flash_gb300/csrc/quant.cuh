@@ -22,7 +22,10 @@
 // block of hb elements, the hb/4 consecutive elements starting at j*hb/4.  The
 // first log2(hb/4) butterfly stages run in registers, the last two exchange
 // with lane j ^ 1 and j ^ 2 by shuffles (the lower element of a pair computes
-// a + b, the upper a - b, exactly as above).
+// a + b, the upper a - b, exactly as above, each as one sign-selected fma).
+// From the second stage on, elements 2k and 2k+1 of a segment always meet the
+// same partner offset, so the stages run on packed f32x2 pairs: the same fp32
+// operations, two per instruction.
 #pragma once
 
 #include <cstdint>
@@ -84,11 +87,17 @@ __device__ __forceinline__ void quant_load(const void* x, int64_t v, int64_t n_v
   }
 }
 
-// One butterfly stage whose partner element sits in lane (lane ^ m): the
-// lower element of the pair (lane bit m clear) gets a + b, the upper a - b.
-__device__ __forceinline__ float xlane_butterfly(float mine, int lane, int m) {
-  const float other = __shfl_xor_sync(0xffffffffu, mine, m);
-  return (lane & m) ? other - mine : mine + other;
+// One butterfly stage, for two packed elements, whose partner elements sit in
+// lane (lane ^ m): the lower element of a pair (lane bit m clear) gets a + b,
+// the upper a - b, both as fma(mine, +-1, other), which rounds exactly like
+// the add or the subtraction.  `sg2` holds +1 twice in the lower lane and -1
+// twice in the upper one.
+__device__ __forceinline__ uint64_t xlane_butterfly2(uint64_t mine, uint64_t sg2, int m) {
+  uint32_t lo, hi;
+  f32x2_unpack(mine, lo, hi);
+  const uint64_t other = f32x2_pack(__uint_as_float(__shfl_xor_sync(0xffffffffu, lo, m)),
+                                    __uint_as_float(__shfl_xor_sync(0xffffffffu, hi, m)));
+  return fma_f32x2(mine, sg2, other);
 }
 
 template <int D>
@@ -97,22 +106,43 @@ __device__ __forceinline__ void quant_rotate(float (&r)[QuantLayout<D>::kPerLane
 #pragma unroll
   for (int c = 0; c < L::kBlocks; ++c) {
     float* b = &r[c * L::kSeg];
-    // stages h = 1 .. kSeg/2 inside the lane's segment
+    // stage h = 1 inside the lane's segment
 #pragma unroll
-    for (int h = 1; h < L::kSeg; h *= 2) {
+    for (int i = 0; i < L::kSeg; i += 2) {
+      const float a = b[i], e = b[i + 1];
+      b[i] = a + e;
+      b[i + 1] = a - e;
+    }
+    // stages h = 2 .. kSeg/2: elements 2k and 2k+1 have the same partner
+    // offset, so each pair of pairs is one packed add and one packed
+    // subtraction (the same fp32 operations, two at a time)
+    uint64_t pk[L::kSeg / 2];
 #pragma unroll
-      for (int i = 0; i < L::kSeg; ++i)
-        if ((i & h) == 0) {
-          const float a = b[i], e = b[i + h];
-          b[i] = a + e;
-          b[i + h] = a - e;
+    for (int k = 0; k < L::kSeg / 2; ++k) pk[k] = f32x2_pack(b[2 * k], b[2 * k + 1]);
+#pragma unroll
+    for (int h2 = 1; h2 < L::kSeg / 2; h2 *= 2) {
+#pragma unroll
+      for (int k = 0; k < L::kSeg / 2; ++k)
+        if ((k & h2) == 0) {
+          const uint64_t a = pk[k], e = pk[k + h2];
+          pk[k] = add_f32x2(a, e);
+          pk[k + h2] = sub_f32x2(a, e);
         }
     }
     // stages h = kSeg, 2 kSeg: partner lane j ^ 1, j ^ 2 (vector-local lane j = lane & 3)
 #pragma unroll
     for (int m = 1; m < kQuantLanes; m *= 2) {
+      const float sg = (lane & m) ? -1.0f : 1.0f;
+      const uint64_t sg2 = f32x2_pack(sg, sg);
 #pragma unroll
-      for (int i = 0; i < L::kSeg; ++i) b[i] = xlane_butterfly(b[i], lane, m);
+      for (int k = 0; k < L::kSeg / 2; ++k) pk[k] = xlane_butterfly2(pk[k], sg2, m);
+    }
+#pragma unroll
+    for (int k = 0; k < L::kSeg / 2; ++k) {
+      uint32_t lo, hi;
+      f32x2_unpack(pk[k], lo, hi);
+      b[2 * k] = __uint_as_float(lo);
+      b[2 * k + 1] = __uint_as_float(hi);
     }
   }
 }
