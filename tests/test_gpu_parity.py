@@ -169,6 +169,28 @@ def test_repeated_launches_are_bitwise_identical():
         assert torch.equal(first, again)
 
 
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_BLOCK_EXACT,
+                                     fa.ATTN_VARIANT_BF16])
+@pytest.mark.parametrize("causal", [True, False])
+def test_every_variant_is_deterministic(variant, causal):
+    """Every path, causal or not, with fp32 output and the log-sum-exp: 20
+    launches on a multi-wave grid give the same bits (no atomics, a fixed
+    accumulation order)."""
+    if variant == fa.ATTN_VARIANT_BF16:
+        b = wl.bf16_gaussian_case(2, 16, 4, 3000, 128, 128)
+        args = dev_bf16(b)
+    else:
+        c = wl.fp8_gaussian_case(2, 16, 4, 3000, 128, 128, seeds=(67, 68, 69))
+        q, k, v, d = dev_fp8(c)
+        args = (q, k, v, *d)
+    first = [t.clone() for t in fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32,
+                                                  causal=causal, return_lse=True)]
+    for _ in range(20):
+        again = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
+                                 return_lse=True)
+        assert all(torch.equal(x, y) for x, y in zip(first, again))
+
+
 # ------------------------------------------------------------------ failure paths
 
 def test_stalled_loads_report_timeout_and_context_survives():
