@@ -18,7 +18,8 @@
  * over all j < S; with ATTN_FLAG_DESCALE_PER_BKV the descales are per (batch,
  * kv head)).
  *
- * Three arithmetic paths compute it:
+ * Four arithmetic paths compute it (the fourth, a diagnostic, through
+ * attn_fwd_ex / attn_fwd_full only):
  *   - attn_fwd_fp8: the Lean-P path.  Each probability is an e4m3 code made by
  *     one multiply-add and an integer conversion ("Lean P: one multiply-add
  *     instead of an exponential"); each 64-key block of probabilities carries
@@ -28,6 +29,10 @@
  *   - attn_fwd_fp8_exact: the exact-softmax FP8 ablation (exact exponential,
  *     probabilities rounded to e4m3, row sum of the unrounded probabilities).
  *   - attn_fwd_bf16: exact softmax with BF16 inputs and probabilities.
+ *   - ATTN_VARIANT_BLOCK_EXACT: Lean-P's block scale and rounded row sum, with
+ *     each probability taken from the exponential unit and rounded to e4m3.
+ * attn_quantize_fp8 turns bf16 or fp32 Q or K into the e4m3 codes and the
+ * device descale these calls take, optionally after a Hadamard rotation.
  *
  * Layouts (all row-major, contiguous, "BSHD" as in flash_attn_func):
  *   q   [B, S, Hq,  Dqk]    k [B, S, Hkv, Dqk]    v [B, S, Hkv, Dv]
