@@ -4,6 +4,7 @@ Small and ragged shapes are compared on every row; the invariants of the
 method (rounded row sum, causality, head mapping, determinism) are checked
 bitwise where they are exact.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -227,3 +228,53 @@ def test_argument_errors_are_reported():
     with pytest.raises(fa.AttnError) as e:
         fa.attn_fwd_fp8(q64, k64, v, *d)
     assert e.value.status == fa.ATTN_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ out-of-bounds writes
+
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16])
+@pytest.mark.parametrize("S,causal", [(1, True), (65, True), (300, False), (257, True)])
+@pytest.mark.parametrize("out_dtype", [fa.ATTN_OUT_BF16, fa.ATTN_OUT_F32])
+def test_no_write_outside_output_and_lse(variant, S, causal, out_dtype):
+    """The output and log-sum-exp are views into larger buffers filled with a
+    canary byte: every byte before and after the views must be untouched, and
+    every element of the views must have been written (no canary left)."""
+    B, Hq, Hkv = 1, 4, 2
+    if variant == fa.ATTN_VARIANT_BF16:
+        args = dev_bf16(wl.bf16_gaussian_case(B, Hq, Hkv, S, 128, 128))
+    else:
+        q, k, v, d = dev_fp8(wl.fp8_gaussian_case(B, Hq, Hkv, S, 128, 128, seeds=(70, 71, 72)))
+        args = (q, k, v, *d)
+    esz = 4 if out_dtype == fa.ATTN_OUT_F32 else 2
+    n_out = B * S * Hq * 128 * esz
+    pad = 4096
+    raw = torch.full((pad + n_out + pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    dt = torch.float32 if out_dtype == fa.ATTN_OUT_F32 else torch.bfloat16
+    out = raw[pad:pad + n_out].view(dt).view(B, S, Hq, 128)
+    n_lse = B * Hq * S * 4
+    raw_lse = torch.full((pad + n_lse + pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    lse_view = raw_lse[pad:pad + n_lse].view(torch.float32).view(B, Hq, S)
+    lib = fa.load_library()
+    ptrs = [ctypes.c_void_p(t.data_ptr()) for t in args]
+    if variant == fa.ATTN_VARIANT_BF16:
+        ptrs = ptrs + [None, None, None]
+    st = lib.attn_fwd_full(int(variant), *ptrs, ctypes.c_void_p(out.data_ptr()), int(out_dtype),
+                           ctypes.c_void_p(lse_view.data_ptr()), B, Hq, Hkv, S, 128, 128,
+                           int(causal), ctypes.c_float(0.0), 0, None,
+                           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == fa.ATTN_OK, fa.status_string(st)
+    torch.cuda.synchronize()
+    for r in (raw, raw_lse):
+        h = r.cpu().numpy()
+        assert np.all(h[:pad] == 0xA5) and np.all(h[-pad:] == 0xA5)
+    # every output element written: a canary float (0xA5A5A5A5 / 0xA5A5) would be
+    # about -2.9e-16 / -2.9e-16 in bf16; finite outputs of attention on these
+    # inputs never equal it
+    body = raw[pad:pad + n_out].cpu().numpy()
+    words = body.view(np.uint32 if esz == 4 else np.uint16)
+    canary = 0xA5A5A5A5 if esz == 4 else 0xA5A5
+    assert not np.any(words == canary)
+    lse_words = raw_lse[pad:pad + n_lse].cpu().numpy().view(np.uint32)
+    assert not np.any(lse_words == 0xA5A5A5A5)
+    assert torch.isfinite(out.float()).all()
