@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3933796608,
-                    "sources_sha256": "9e5f7c13574bf631339196c5000513c63e2a4c0ef6cb74ffb55a5bdab207d67b"}
+PROFILED_TRAFFIC = {"bytes": 3948403968,
+                    "sources_sha256": "c98b73ccd37462c08e919d03eb62ad781f74b438b1072b94068bd5cea64bc760"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

@@ -22,6 +22,7 @@ import os
 import re
 import threading
 
+import numpy as np
 import torch
 
 from . import _build
@@ -48,6 +49,7 @@ HEADER = os.path.join(_build.ROOT, "include", "fp8attn.h")
 LIBRARY_PATH = _build.SO
 
 _lib = None
+_lib_tl = None
 _lock = threading.Lock()
 
 
@@ -62,6 +64,28 @@ def build(force: bool = False) -> str:
     return _build.build(force=force)
 
 
+def _open(path):
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fp8_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.attn_fwd_fp8.argtypes = fp8_args
+    lib.attn_fwd_fp8_exact.argtypes = fp8_args
+    lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
+    lib.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
+                                vp, vp]
+    lib.attn_quantize_fp8.argtypes = [vp, i, vp, vp, i, i, i, i, i, vp]
+    lib.attn_fwd_full.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
+                                  i, vp, vp]
+    lib.attn_debug_timeline.argtypes = [vp, i, i]
+    for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
+                 "attn_quantize_fp8", "attn_fwd_full", "attn_launches_per_call",
+                 "attn_api_version", "attn_debug_timeline"):
+        getattr(lib, name).restype = ctypes.c_int
+    lib.attn_status_string.argtypes = [i]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    return lib
+
+
 def load_library():
     """Load libfp8attn.so; raise if it has not been built."""
     global _lib
@@ -71,25 +95,28 @@ def load_library():
         if not os.path.exists(LIBRARY_PATH):
             raise RuntimeError(
                 f"{LIBRARY_PATH} is missing: build it with fp8_causal_prefill_flash_gb300.build()")
-        lib = ctypes.CDLL(LIBRARY_PATH)
-        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        fp8_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
-        lib.attn_fwd_fp8.argtypes = fp8_args
-        lib.attn_fwd_fp8_exact.argtypes = fp8_args
-        lib.attn_fwd_bf16.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
-        lib.attn_fwd_ex.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i,
-                                    vp, vp]
-        lib.attn_quantize_fp8.argtypes = [vp, i, vp, vp, i, i, i, i, i, vp]
-        lib.attn_fwd_full.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
-                                      i, vp, vp]
-        for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
-                     "attn_quantize_fp8", "attn_fwd_full", "attn_launches_per_call",
-                     "attn_api_version"):
-            getattr(lib, name).restype = ctypes.c_int
-        lib.attn_status_string.argtypes = [i]
-        lib.attn_status_string.restype = ctypes.c_char_p
-        _lib = lib
-        return lib
+        _lib = _open(LIBRARY_PATH)
+        return _lib
+
+
+def load_timeline_library():
+    """Build (if needed) and load the debug library whose kernels record the
+    clock64 role timeline; its entry points are called through ctypes like
+    the release library's (the Python functions here use the release one)."""
+    global _lib_tl
+    with _lock:
+        if _lib_tl is None:
+            _lib_tl = _open(_build.build(timeline=True))
+        return _lib_tl
+
+
+def debug_timeline(lib, reset: bool = True) -> np.ndarray:
+    """The role timeline of the last call made through ``lib`` (the debug
+    library): uint64 clock64 stamps [4, 64, 8], layout as in fp8attn.h."""
+    buf = np.zeros((4, 64, 8), dtype=np.uint64)
+    st = lib.attn_debug_timeline(buf.ctypes.data, buf.size, int(bool(reset)))
+    _raise(st, "attn_debug_timeline")
+    return buf
 
 
 def declared_functions() -> list[str]:

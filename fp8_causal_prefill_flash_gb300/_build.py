@@ -9,6 +9,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SO = os.path.join(PKG, "libfp8attn.so")
+# debug build with the clock64 role timeline (attn_debug_timeline)
+SO_TIMELINE = os.path.join(PKG, "libfp8attn_timeline.so")
 SOURCES = [os.path.join(CSRC, "api.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd.cuh", "ptx.cuh", "quant.cuh")] + [
     os.path.join(ROOT, "include", "fp8attn.h")]
@@ -22,25 +24,27 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(SO):
+def up_to_date(so: str = SO) -> bool:
+    if not os.path.exists(so):
         return False
-    t = os.path.getmtime(SO)
+    t = os.path.getmtime(so)
     return all(os.path.getmtime(d) <= t for d in DEPS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the CUDA library (skipped when it is newer than its sources)."""
-    if not force and up_to_date():
-        return SO
-    tmp = SO + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, *SOURCES, "-o", tmp]
+def build(force: bool = False, verbose: bool = False, timeline: bool = False) -> str:
+    """Compile the CUDA library (skipped when it is newer than its sources).
+    ``timeline`` builds the separate debug library with the role timeline."""
+    so = SO_TIMELINE if timeline else SO
+    if not force and up_to_date(so):
+        return so
+    tmp = so + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, *(["-DFA8_TIMELINE"] if timeline else []), *SOURCES, "-o", tmp]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), file=sys.stderr)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, SO)
-    return SO
+    os.replace(tmp, so)
+    return so
 
 
 if __name__ == "__main__":

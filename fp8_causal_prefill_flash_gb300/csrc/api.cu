@@ -300,4 +300,27 @@ int attn_launches_per_call(void) { return 1; }
 
 int attn_api_version(void) { return FP8ATTN_API_VERSION; }
 
+int attn_debug_timeline(unsigned long long* host, int capacity, int reset) {
+#ifdef FA8_TIMELINE
+  constexpr int kN = 4 * 64 * 8;
+  if (!host || capacity < 0) return ATTN_ERR_INVALID_ARG;
+  int sms = 0;
+  const int st = device_check(&sms);
+  if (st != ATTN_OK) return st;
+  const int n = capacity < kN ? capacity : kN;
+  if (n > 0 && cudaMemcpyFromSymbol(host, fa8::fa8_timeline, sizeof(unsigned long long) * n) !=
+                   cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (reset) {
+    static const unsigned long long zeros[kN] = {};
+    if (cudaMemcpyToSymbol(fa8::fa8_timeline, zeros, sizeof zeros) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+#else
+  (void)host, (void)capacity, (void)reset;
+  return ATTN_ERR_UNSUPPORTED;
+#endif
+}
+
 }  // extern "C"

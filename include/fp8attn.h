@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 4
+#define FP8ATTN_API_VERSION 5
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -206,6 +206,20 @@ int attn_quantize_fp8(const void* x, int in_dtype, void* codes, float* descale, 
 
 /* Library ABI version (FP8ATTN_API_VERSION of the build). */
 int attn_api_version(void);
+
+/* Debug timeline (only in the debug library built with FA8_TIMELINE; the
+ * release library returns ATTN_ERR_UNSUPPORTED without touching the device).
+ * Copies the clock64 stamps that CTA 0 recorded for its first work item into
+ * host[0 .. min(capacity, 2048)), as [4][64][8] unsigned 64-bit values:
+ *   [t][j][0..4]   softmax of query tile t, key tile j: before the wait for S,
+ *                  S ready, S copied out (arrived), codes computed, P stored
+ *   [2+t][j][0..2] P.V issuer for tile t: before the wait for P, P ready, P.V
+ *                  issued;  [2+t][j][3..5] S issuer for tile t: before the
+ *                  wait for S to be free, S free, S product issued
+ * Unwritten entries are 0 (after a reset) or hold older launches' stamps.
+ * With reset != 0 the device copy is zeroed afterwards.  Synchronous with
+ * respect to the device; for profiling, not for production calls. */
+int attn_debug_timeline(unsigned long long* host, int capacity, int reset);
 
 #ifdef __cplusplus
 }

@@ -18,14 +18,14 @@ def test_header_declares_the_entry_points():
     names = fa.declared_functions()
     for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
               "attn_quantize_fp8", "attn_fwd_full", "attn_status_string",
-              "attn_launches_per_call", "attn_api_version"):
+              "attn_launches_per_call", "attn_api_version", "attn_debug_timeline"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 4
+    assert lib.attn_api_version() == 5
     assert lib.attn_launches_per_call() == 1
 
 
@@ -111,3 +111,11 @@ def test_full_entry_point_checks_arguments(lib):
     assert f(*args(flags=4)) == fa.ATTN_ERR_INVALID_ARG                  # unknown flag
     assert f(*args(causal=-1)) == fa.ATTN_ERR_INVALID_ARG
     assert f(*args(Dv=64, flags=fa.ATTN_FLAG_DESCALE_PER_BKV)) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_release_library_has_no_timeline(lib):
+    """The release build answers the debug timeline call with UNSUPPORTED
+    before touching any device."""
+    import numpy as np
+    buf = np.zeros(16, dtype=np.uint64)
+    assert lib.attn_debug_timeline(buf.ctypes.data, buf.size, 1) == fa.ATTN_ERR_UNSUPPORTED
