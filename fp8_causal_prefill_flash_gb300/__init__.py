@@ -59,9 +59,10 @@ class AttnError(RuntimeError):
         self.status = status
 
 
-def build(force: bool = False) -> str:
-    """Compile libfp8attn.so in-tree (nvcc, sm_103a)."""
-    return _build.build(force=force)
+def build(force: bool = False, timeline: bool = False) -> str:
+    """Compile libfp8attn.so in-tree (nvcc, sm_103a); ``timeline`` builds the
+    debug library libfp8attn_timeline.so instead."""
+    return _build.build(force=force, timeline=timeline)
 
 
 def _open(path):
@@ -87,8 +88,12 @@ def _open(path):
 
 
 def load_library():
-    """Load libfp8attn.so; raise if it has not been built."""
+    """Load libfp8attn.so; raise if it has not been built.  With the
+    environment variable FP8ATTN_TIMELINE=1 every call goes to the debug
+    library with the role timeline instead (see debug_timeline)."""
     global _lib
+    if os.environ.get("FP8ATTN_TIMELINE") == "1":
+        return load_timeline_library()
     with _lock:
         if _lib is not None:
             return _lib
