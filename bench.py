@@ -404,11 +404,6 @@ def run_ours(args, rank, world, local_rank):
     e_end = meter.read_mj()
     clk = clocks.stop()
     h_timed = output_sha256(out)
-    if args.leanp_only:
-        if rank == 0:
-            print(json.dumps({"workload": workload, "S": S, "ms_per_step": ms,
-                              "tflops": F / (ms * 1e-3) / 1e12}), flush=True)
-        return 0
 
     # exact-softmax FP8 ablation, same workload
     def step_abl():
@@ -831,8 +826,6 @@ def main():
                     help="DRAM bytes per launch from an ncu capture of the same kernel")
     ap.add_argument("--workload", default=WORKLOAD, help="configuration name (profiling)")
     ap.add_argument("--S", type=int, default=None, help="override the sequence length (profiling)")
-    ap.add_argument("--leanp-only", action="store_true",
-                    help="time only the Lean-P kernel and print a short line (profiling)")
     ap.add_argument("--only", choices=list(ONLY_PATHS), default=None,
                     help="time one kernel alone on its workload (profiling)")
     ap.add_argument("--cpu-sweep", action="store_true",
