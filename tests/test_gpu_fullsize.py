@@ -159,3 +159,52 @@ def test_sink_input():
           f"ratio {e_lp / e_ab:.3f}")
     assert e_lp <= FP8_RMS_TOL
     assert e_lp <= 0.5 * e_ab
+
+
+def test_noncausal_fullsize_with_per_bkv_descales():
+    """The non-causal call the sweep times on the C2 shape (every row sees all
+    S keys), here with descales per (batch, kv head): Lean-P output and LSE
+    against the oracle's non-causal definition on sampled rows."""
+    case = wl.make_case("fp8_gqa_h32_8_s16k_d128_outliers")
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    rng = np.random.default_rng(210)
+    dq, dk, dv = (x * rng.uniform(0.5, 2.0, (B, Hkv)) for x in (case.dq, case.dk, case.dv))
+    q, k, v = (torch.from_numpy(a).cuda() for a in (case.q, case.k, case.v))
+    d = [torch.from_numpy(np.asarray(x, np.float32).reshape(-1).copy()).cuda() for x in (dq, dk, dv)]
+    out, lse = fa.attn_fwd_full(fa.ATTN_VARIANT_LEANP, q, k, v, *d, out_dtype=fa.ATTN_OUT_F32,
+                                causal=False, return_lse=True)
+    torch.cuda.synchronize()
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    del q, k, v
+    torch.cuda.empty_cache()
+    rows = sample_rows(B, Hq, S, n_random=64, seed=3)
+    emul, amb, lse_e = oracle.attention("leanp", case.q, case.k, case.v, dq, dk, dv, rows=rows,
+                                        causal=False)
+    ref, _, _ = oracle.attention("ref", case.q, case.k, case.v, dq, dk, dv, rows=rows,
+                                 causal=False)
+    gpu = pick(out, rows)
+    vmax = float(np.max(np.abs(oracle.e4m3_decode(case.v)))) * float(np.max(dv))
+    check_rows(gpu, emul, amb, vmax)
+    glse = np.array([lse[b, h, i] for b, h, i in rows], dtype=np.float64)
+    a = np.minimum(amb, 0.5)
+    assert np.all(np.abs(glse - lse_e) <= 2e-5 * (1 + np.abs(lse_e)) + 2.0 * a / (1.0 - a))
+    assert rel_rms(gpu, ref) <= FP8_RMS_TOL
+    assert np.isfinite(out).all()
+
+
+def test_noncausal_bf16_fullsize():
+    case = wl.make_case("bf16_gqa_h32_8_s16k_d128")
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    q, k, v = (torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+               for a in (case.q, case.k, case.v))
+    out = fa.attn_fwd_full(fa.ATTN_VARIANT_BF16, q, k, v, out_dtype=fa.ATTN_OUT_F32, causal=False)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy()
+    rows = sample_rows(B, Hq, S, n_random=64, seed=4)
+    gpu = pick(out, rows)
+    emul, _, _ = oracle.attention("bf16", case.q, case.k, case.v, rows=rows, causal=False)
+    ref, _, _ = oracle.attention("ref_bf16", case.q, case.k, case.v, rows=rows, causal=False)
+    vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
+    assert np.max(np.abs(gpu - emul)) <= EMUL_TOL * vmax
+    assert rel_rms(gpu, ref) <= BF16_RMS_TOL
+    assert np.isfinite(out).all()
