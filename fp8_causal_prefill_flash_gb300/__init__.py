@@ -42,6 +42,7 @@ ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 ATTN_FLAG_TEST_STALL_LOADS = 1
 ATTN_FLAG_DESCALE_PER_BKV = 2
+ATTN_FLAG_TEST_CHUNK_UNITS = 4
 ATTN_IN_BF16 = 0
 ATTN_IN_F32 = 1
 

@@ -21,6 +21,11 @@ using fa8::Maps;
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;      // 4 s per wait
 constexpr unsigned long long kTestWaitLimitNs = 200000000ull;   // 0.2 s (stall test)
 constexpr int kMaxDevices = 64;
+// Item chunking thresholds (bytes of K and V): above kChunkAllBytes for the
+// whole problem, chunks hold about kChunkBytes, half of the 129 MB L2, so
+// that the two or three chunks' worth of kv heads in flight stay in L2.
+constexpr size_t kChunkAllBytes = 512ull << 20;
+constexpr size_t kChunkBytes = 64ull << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -127,7 +132,8 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale)) return ATTN_ERR_INVALID_ARG;
   if ((flags & ATTN_FLAG_TEST_STALL_LOADS) && !dev_status) return ATTN_ERR_INVALID_ARG;
-  if (flags & ~(ATTN_FLAG_TEST_STALL_LOADS | ATTN_FLAG_DESCALE_PER_BKV)) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~(ATTN_FLAG_TEST_STALL_LOADS | ATTN_FLAG_DESCALE_PER_BKV | ATTN_FLAG_TEST_CHUNK_UNITS))
+    return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   if (Dv != 128) return ATTN_ERR_UNSUPPORTED;
@@ -159,6 +165,22 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   p.status = dev_status;
   p.flags = flags;
   p.wait_limit_ns = (flags & ATTN_FLAG_TEST_STALL_LOADS) ? kTestWaitLimitNs : kWaitLimitNs;
+  // Item chunks (see decode_item): one chunk while the K and V of all
+  // (batch, kv head) units take at most kChunkAllBytes; beyond that, chunks
+  // of about kChunkBytes of K and V each (at least one unit).
+  {
+    const size_t kv_unit = (size_t)S * (size_t)(Dqk + Dv) * (size_t)(fp8 ? 1 : 2);
+    const long long units = (long long)B * Hkv;
+    long long g = units;
+    if (flags & ATTN_FLAG_TEST_CHUNK_UNITS) {
+      g = 1;
+    } else if (kv_unit * (size_t)units > kChunkAllBytes) {
+      g = (long long)(kChunkBytes / kv_unit);
+      if (g < 1) g = 1;
+      if (g > units) g = units;
+    }
+    p.chunk_q = (int)(g * (Hq / Hkv));
+  }
   p.causal = causal;
   p.descale_per_bkv = (flags & ATTN_FLAG_DESCALE_PER_BKV) ? 1 : 0;
   p.lse = lse;

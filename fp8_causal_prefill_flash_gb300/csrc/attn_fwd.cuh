@@ -139,6 +139,7 @@ struct KParams {
   int* status;       // optional device status word
   int flags;
   unsigned long long wait_limit_ns;
+  int chunk_q;         // query-head units (b, h) per item chunk, a multiple of Hq / Hkv
   int causal;          // 1: keys j <= i; 0: all S keys
   int descale_per_bkv; // descales hold one value per (batch, kv head) instead of one
   float* lse;          // optional [B, Hq, S] natural-log row sums (nullptr: none)
@@ -158,12 +159,23 @@ __device__ __forceinline__ int item_at(int round, int n_items) {
   return pos < n_items ? pos : -1;
 }
 
+// Item order: the query-head units q = b*Hq + h are split into chunks of
+// chunk_q consecutive units (whole kv heads); chunks run one after another,
+// and inside a chunk the query blocks run longest first with the units as the
+// fast index.  One chunk (chunk_q = B*Hq) is the plain longest-first order.
+// Smaller chunks keep the CTAs in flight on few kv heads, so that their K and
+// V tiles are shared in L2 when all heads' K and V would not fit there.
 __device__ __forceinline__ void decode_item(const KParams& p, int idx, int& b, int& h, int& qb) {
-  const int per_qb = p.B * p.Hq;
-  qb = p.n_qblocks - 1 - idx / per_qb;
-  const int r = idx % per_qb;
-  b = r / p.Hq;
-  h = r % p.Hq;
+  const int units = p.B * p.Hq;
+  const int per_chunk = p.chunk_q * p.n_qblocks;
+  const int c = idx / per_chunk;
+  const int q0 = c * p.chunk_q;
+  const int cq = units - q0 < p.chunk_q ? units - q0 : p.chunk_q;
+  const int li = idx - c * per_chunk;
+  qb = p.n_qblocks - 1 - li / cq;
+  const int q = q0 + li % cq;
+  b = q / p.Hq;
+  h = q % p.Hq;
 }
 
 // Number of key tiles query tile t of block qb needs (keys < min(S, last row + 1)).

@@ -59,7 +59,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 5
+#define FP8ATTN_API_VERSION 6
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -100,6 +100,11 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
  * of kv head g in batch b use entry b*Hkv + g (the per-(batch, kv head)
  * descales of FP8 flash_attn_func); without the flag, one value each. */
 #define ATTN_FLAG_DESCALE_PER_BKV 2
+/* Test hook: run the work items in chunks of one (batch, kv head) each, the
+ * order the library otherwise chooses only for problems whose K and V exceed
+ * 512 MB (to keep the kv heads in flight inside L2).  The item order changes
+ * no arithmetic, so the result is bitwise the same as without the flag. */
+#define ATTN_FLAG_TEST_CHUNK_UNITS 4
 
 /*
  * FP8 Lean-P causal prefill attention ("Lean P: one multiply-add instead of an
@@ -160,7 +165,8 @@ int attn_launches_per_call(void);
  * FlashAttention for AMD MI355X", "TL;DR").
  *   causal     1: row i sees keys 0 .. i; 0: every row sees all S keys
  *   flags      ATTN_FLAG_DESCALE_PER_BKV for [B, Hkv] descales (FP8 only);
- *              ATTN_FLAG_TEST_STALL_LOADS as for attn_fwd_ex
+ *              ATTN_FLAG_TEST_STALL_LOADS, ATTN_FLAG_TEST_CHUNK_UNITS as for
+ *              attn_fwd_ex
  *   lse        NULL, or a device pointer to fp32 [B, Hq, S] (4-byte aligned):
  *              lse[b,h,i] = ln sum_j w_ij, the natural log of the row's own
  *              unnormalised weights (Lean-P: the rounded, scaled weights whose

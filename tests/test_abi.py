@@ -25,7 +25,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 5
+    assert lib.attn_api_version() == 6
     assert lib.attn_launches_per_call() == 1
 
 
@@ -62,6 +62,7 @@ def call_ex(lib, variant=0, q=P, k=P, v=P, dq=P, dk=P, dv=P, out=P, out_dtype=0,
     (dict(scale=float("nan")), fa.ATTN_ERR_INVALID_ARG),
     (dict(causal=2), fa.ATTN_ERR_INVALID_ARG),
     (dict(flags=8), fa.ATTN_ERR_INVALID_ARG),          # unknown flag
+    (dict(flags=16), fa.ATTN_ERR_INVALID_ARG),         # unknown flag
     (dict(Dqk=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(Dv=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(variant=2, Dqk=192), fa.ATTN_ERR_UNSUPPORTED),
@@ -108,7 +109,7 @@ def test_full_entry_point_checks_arguments(lib):
                          128, 128, kw.get("Dv", 128), kw.get("causal", 1), 0.0, kw.get("flags", 0),
                          None, None]
     assert f(*args(lse=MIS)) == fa.ATTN_ERR_INVALID_ARG                  # misaligned lse
-    assert f(*args(flags=4)) == fa.ATTN_ERR_INVALID_ARG                  # unknown flag
+    assert f(*args(flags=8)) == fa.ATTN_ERR_INVALID_ARG                  # unknown flag
     assert f(*args(causal=-1)) == fa.ATTN_ERR_INVALID_ARG
     assert f(*args(Dv=64, flags=fa.ATTN_FLAG_DESCALE_PER_BKV)) == fa.ATTN_ERR_UNSUPPORTED
 

@@ -67,3 +67,31 @@ def test_output_past_2_31_elements():
     print(f"max-size rows: Lean-P rel-RMS vs fp64 {err:.4f}")
     # diffuse Gaussian rows of 64K-131K keys: the scheme's own error (about 3.2e-2)
     assert err <= 3.5e-2
+
+
+def test_long_sequence_chunked_order():
+    """B=1, 32 heads, S=131072 at d128: K and V of all heads take 2 GB, so the
+    library runs the items in chunks of two kv heads (64 MB of K and V each).
+    Sampled rows of several heads against the oracle, the longest prefixes
+    included."""
+    fa.build()
+    fa.load_library()
+    H, S = 32, 131072
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2025)
+    q, dq = _codes((1, S, H, D), gen)
+    k, dk = _codes((1, S, H, D), gen)
+    v, dv = _codes((1, S, H, D), gen)
+    d = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in (dq, dk, dv)]
+    out = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d, out_dtype=fa.ATTN_OUT_F32)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all().item())
+    rng = np.random.default_rng(9)
+    for h in (0, 13, H - 1):
+        rows = sorted({0, 255, 256, S // 2, S - 129, S - 1} | {int(x) for x in rng.integers(0, S, 3)})
+        qh, kh, vh = (t[:, :, h:h + 1, :].contiguous().cpu().numpy() for t in (q, k, v))
+        r = np.array([(0, 0, i) for i in rows], dtype=np.int64)
+        emul, amb, _ = oracle.attention("leanp", qh, kh, vh, dq, dk, dv, rows=r)
+        gpu = out[0, torch.tensor(rows, device="cuda"), h].cpu().numpy().astype(np.float64)
+        vmax = float(np.max(np.abs(oracle.e4m3_decode(vh)))) * dv
+        check_rows(gpu, emul, amb, vmax, EMUL_TOL)

@@ -278,3 +278,26 @@ def test_no_write_outside_output_and_lse(variant, S, causal, out_dtype):
     lse_words = raw_lse[pad:pad + n_lse].cpu().numpy().view(np.uint32)
     assert not np.any(lse_words == 0xA5A5A5A5)
     assert torch.isfinite(out.float()).all()
+
+
+# ------------------------------------------------------------------ item order
+
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16])
+@pytest.mark.parametrize("causal", [True, False])
+def test_chunked_item_order_gives_the_same_bits(variant, causal):
+    """Work items chunked by (batch, kv head), the order used for problems
+    whose K and V exceed L2, against the plain longest-first order: the same
+    output and log-sum-exp bit for bit, on a multi-wave grid with B = 2 and
+    GQA."""
+    if variant == fa.ATTN_VARIANT_BF16:
+        args = dev_bf16(wl.bf16_gaussian_case(2, 12, 3, 2100, 128, 128))
+    else:
+        q, k, v, d = dev_fp8(wl.fp8_gaussian_case(2, 12, 3, 2100, 128, 128, seeds=(73, 74, 75)))
+        args = (q, k, v, *d)
+    plain = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
+                             return_lse=True)
+    chunked = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
+                               return_lse=True, flags=fa.ATTN_FLAG_TEST_CHUNK_UNITS)
+    torch.cuda.synchronize()
+    assert torch.equal(plain[0], chunked[0]) and torch.equal(plain[1], chunked[1])
