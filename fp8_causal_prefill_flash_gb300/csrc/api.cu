@@ -24,7 +24,7 @@ constexpr int kMaxDevices = 64;
 // Item chunking thresholds (bytes of K and V): above kChunkAllBytes for the
 // whole problem, chunks hold about kChunkBytes, half of the 129 MB L2, so
 // that the two or three chunks' worth of kv heads in flight stay in L2.
-constexpr size_t kChunkAllBytes = 512ull << 20;
+constexpr size_t kChunkAllBytes = 256ull << 20;
 constexpr size_t kChunkBytes = 64ull << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

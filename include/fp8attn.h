@@ -102,7 +102,7 @@ typedef enum { ATTN_OUT_BF16 = 0, ATTN_OUT_F32 = 1 } attn_out_dtype;
 #define ATTN_FLAG_DESCALE_PER_BKV 2
 /* Test hook: run the work items in chunks of one (batch, kv head) each, the
  * order the library otherwise chooses only for problems whose K and V exceed
- * 512 MB (to keep the kv heads in flight inside L2).  The item order changes
+ * 256 MB (to keep the kv heads in flight inside L2).  The item order changes
  * no arithmetic, so the result is bitwise the same as without the flag. */
 #define ATTN_FLAG_TEST_CHUNK_UNITS 4
 
