@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3948403968,
-                    "sources_sha256": "c98b73ccd37462c08e919d03eb62ad781f74b438b1072b94068bd5cea64bc760"}
+PROFILED_TRAFFIC = {"bytes": 3938462208,
+                    "sources_sha256": "d75df494bf49dfb22e915948f3f4e3ebe2ce9a3e0af43a1f69d31ba72b9a7881"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")
