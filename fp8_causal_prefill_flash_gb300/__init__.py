@@ -51,6 +51,7 @@ LIBRARY_PATH = _build.SO
 
 _lib = None
 _lib_tl = None
+_TIMELINE = os.environ.get("FP8ATTN_TIMELINE") == "1"
 _lock = threading.Lock()
 
 
@@ -90,10 +91,13 @@ def _open(path):
 
 def load_library():
     """Load libfp8attn.so; raise if it has not been built.  With the
-    environment variable FP8ATTN_TIMELINE=1 every call goes to the debug
-    library with the role timeline instead (see debug_timeline)."""
+    environment variable FP8ATTN_TIMELINE=1 (read when the package is
+    imported) every call goes to the debug library with the role timeline
+    instead (see debug_timeline)."""
     global _lib
-    if os.environ.get("FP8ATTN_TIMELINE") == "1":
+    if _lib is not None:
+        return _lib
+    if _TIMELINE:
         return load_timeline_library()
     with _lock:
         if _lib is not None:
@@ -138,11 +142,23 @@ def status_string(status: int) -> str:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream_handle():
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+# torch's raw current-stream query (no Stream object); the public API otherwise
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_handle(t=None):
+    """The current CUDA stream as a plain integer handle.  The library launches
+    on the current device, so t (the call's first tensor) must live there."""
+    dev = torch.cuda.current_device()
+    if t is not None and t.get_device() != dev:
+        raise ValueError(f"tensors are on cuda:{t.get_device()} but the current device is "
+                         f"cuda:{dev}; call inside torch.cuda.device({t.get_device()})")
+    if _raw_stream is not None:
+        return _raw_stream(dev)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check_qkv(q, k, v, fp8: bool):
@@ -189,7 +205,7 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, out=None, causal=True
     out = _out(out, q, Dv, torch.bfloat16)
     st = lib.attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
                           _ptr(descale_v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv, int(bool(causal)),
-                          _stream_handle())
+                          _stream_handle(q))
     _raise(st, "attn_fwd_fp8")
     return out
 
@@ -203,7 +219,7 @@ def attn_fwd_fp8_exact(q, k, v, descale_q, descale_k, descale_v, out=None, causa
     out = _out(out, q, Dv, torch.bfloat16)
     st = lib.attn_fwd_fp8_exact(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
                                 _ptr(descale_v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv,
-                                int(bool(causal)), _stream_handle())
+                                int(bool(causal)), _stream_handle(q))
     _raise(st, "attn_fwd_fp8_exact")
     return out
 
@@ -214,7 +230,7 @@ def attn_fwd_bf16(q, k, v, out=None, causal=True):
     B, Hq, Hkv, S, Dqk, Dv = _check_qkv(q, k, v, False)
     out = _out(out, q, Dv, torch.bfloat16)
     st = lib.attn_fwd_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, S, Dqk, Dv,
-                           int(bool(causal)), _stream_handle())
+                           int(bool(causal)), _stream_handle(q))
     _raise(st, "attn_fwd_bf16")
     return out
 
@@ -235,7 +251,7 @@ def attn_fwd_ex(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None
     st = lib.attn_fwd_ex(int(variant), _ptr(q), _ptr(k), _ptr(v), _ptr(descale_q),
                          _ptr(descale_k), _ptr(descale_v), _ptr(out), int(out_dtype), B, Hq, Hkv,
                          S, Dqk, Dv, int(bool(causal)), float(softmax_scale), int(flags),
-                         _ptr(dev_status), _stream_handle())
+                         _ptr(dev_status), _stream_handle(q))
     if raise_on_error:
         _raise(st, "attn_fwd_ex")
         return out
@@ -267,7 +283,7 @@ def attn_quantize_fp8(x, hadamard=False, codes=None, descale=None):
     if descale.dtype != torch.float32 or descale.numel() != 1:
         raise ValueError("descale must be a one-element float32 tensor")
     st = lib.attn_quantize_fp8(_ptr(x), in_dtype, _ptr(codes), _ptr(descale), B, S, H, D,
-                               int(bool(hadamard)), _stream_handle())
+                               int(bool(hadamard)), _stream_handle(x))
     _raise(st, "attn_quantize_fp8")
     return codes, descale
 
@@ -297,7 +313,7 @@ def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=No
     st = lib.attn_fwd_full(variant, _ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
                            _ptr(descale_v), _ptr(out), out_dtype, _ptr(lse), B, Hq, Hkv, S, Dqk,
                            Dv, int(bool(causal)), float(softmax_scale or 0.0), flags,
-                           _ptr(dev_status), _stream_handle())
+                           _ptr(dev_status), _stream_handle(q))
     _raise(st, "attn_fwd_full")
     return (out, lse) if return_lse else out
 
