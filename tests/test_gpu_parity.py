@@ -170,6 +170,24 @@ def test_repeated_launches_are_bitwise_identical():
         assert torch.equal(first, again)
 
 
+def test_bitwise_identical_over_7200_launches():
+    """The articles report bitwise-identical output over 7,200 launches
+    ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X", "How accurate is
+    ZYFA's FP8 attention?").  Here: 7,200 Lean-P launches of a 3.4-wave
+    problem (B=1, 32 heads, S=4096), each compared with the first on the
+    device."""
+    case = wl.fp8_gaussian_case(1, 32, 32, 4096, 128, 128, seeds=(76, 77, 78))
+    q, k, v, d = dev_fp8(case)
+    first = fa.attn_fwd_fp8(q, k, v, *d).clone()
+    out = torch.empty_like(first)
+    diff = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for _ in range(7200):
+        fa.attn_fwd_fp8(q, k, v, *d, out=out)
+        diff += (out.view(torch.int16) != first.view(torch.int16)).sum()
+    torch.cuda.synchronize()
+    assert diff.item() == 0
+
+
 @pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_BLOCK_EXACT,
                                      fa.ATTN_VARIANT_BF16])
 @pytest.mark.parametrize("causal", [True, False])
