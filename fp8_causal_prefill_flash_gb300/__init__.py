@@ -334,6 +334,22 @@ def flash_attn_fp8_func(q, k, v, q_descale=None, k_descale=None, v_descale=None,
                          return_lse=return_softmax_lse)
 
 
+def flash_attn_fp8_from_bf16(q, k, v, hadamard=True, softmax_scale=None, causal=True,
+                             return_softmax_lse=False):
+    """Lean-P attention on bf16 (or fp32) activations: Q and K are quantised
+    per tensor to e4m3, after the Hadamard rotation when ``hadamard`` is set
+    (it leaves Q K^T unchanged and spreads outlier channels, "Zyphra ZYFA: FP8
+    FlashAttention for AMD MI355X", "How accurate is ZYFA's FP8 attention?"),
+    V is quantised as it is, and the three codes and descales go to the
+    Lean-P kernel.  Four library calls on the current stream; the codes are
+    new tensors."""
+    cq, dq = attn_quantize_fp8(q, hadamard=hadamard)
+    ck, dk = attn_quantize_fp8(k, hadamard=hadamard)
+    cv, dv = attn_quantize_fp8(v, hadamard=False)
+    return flash_attn_fp8_func(cq, ck, cv, dq, dk, dv, softmax_scale=softmax_scale, causal=causal,
+                               return_softmax_lse=return_softmax_lse)
+
+
 def flash_attn_bf16_func(q, k, v, softmax_scale=None, causal=True, return_softmax_lse=False):
     """flash_attn_func-style call on bf16 inputs (exact softmax)."""
     return attn_fwd_full(ATTN_VARIANT_BF16, q, k, v, causal=causal, softmax_scale=softmax_scale,
