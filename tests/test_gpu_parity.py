@@ -319,3 +319,30 @@ def test_chunked_item_order_gives_the_same_bits(variant, causal):
                                return_lse=True, flags=fa.ATTN_FLAG_TEST_CHUNK_UNITS)
     torch.cuda.synchronize()
     assert torch.equal(plain[0], chunked[0]) and torch.equal(plain[1], chunked[1])
+
+
+# ------------------------------------------------------------------ extreme ranges
+
+@pytest.mark.parametrize("spread", [50.0, 300.0])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+def test_extreme_logit_ranges(spread, variant):
+    """Descales that spread the logits over hundreds of nats: the lazy
+    reference must move by exact powers of two, far-below blocks clamp their
+    UE8M0 factor, and the ablation flushes tiny probabilities; the output still
+    matches the oracle's emulation under the per-row gate and stays finite."""
+    case = wl.fp8_gaussian_case(1, 2, 2, 700, 128, 128, seeds=(79, 80, 81))
+    # logit standard deviation ~ spread nats: scale dq*dk accordingly
+    q8 = oracle.e4m3_decode(case.q) * case.dq
+    k8 = oracle.e4m3_decode(case.k) * case.dk
+    s_std = float(np.std(np.einsum("bshd,bthd->bhst", q8[:, :64], k8[:, :64])))
+    f = spread / (s_std / np.sqrt(128.0))
+    dq, dk = case.dq * np.sqrt(f), case.dk * np.sqrt(f)
+    q, k, v, _ = dev_fp8(case)
+    d = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in (dq, dk, case.dv)]
+    out = fa.attn_fwd_ex(variant, q, k, v, *d)
+    torch.cuda.synchronize()
+    gpu = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(gpu).all()
+    path = "leanp" if variant == fa.ATTN_VARIANT_LEANP else "exact_fp8"
+    emul, amb, _ = oracle.attention(path, case.q, case.k, case.v, dq, dk, case.dv)
+    check_rows(gpu.reshape(-1, 128), emul.reshape(-1, 128), amb.reshape(-1), vmax_fp8(case))
