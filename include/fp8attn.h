@@ -41,6 +41,12 @@
  * DEVICE memory (per-tensor descales), so a call can be captured in a CUDA
  * graph.  BF16 inputs are bf16 values.
  *
+ * Non-finite codes: e4m3 has no infinities; a NaN code (0x7F, 0xFF) in q or k
+ * makes that score NaN.  The Lean-P path gives such a key weight 0 (its
+ * saturating multiply-add flushes NaN to 0 and the block maximum skips it);
+ * the exact paths propagate the NaN to every row that sees the key.  A NaN in
+ * v reaches every row whose weight on that key is non-zero.
+ *
  * Supported: causal = 0 or 1, (Dqk, Dv) in {(128, 128), (192, 128)} for FP8 and
  * (128, 128) for BF16, any S >= 1, B >= 1, Hq % Hkv == 0.  Base addresses must
  * be 16-byte aligned.  The device must be sm_103 (GB300).

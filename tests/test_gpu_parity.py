@@ -346,3 +346,19 @@ def test_extreme_logit_ranges(spread, variant):
     path = "leanp" if variant == fa.ATTN_VARIANT_LEANP else "exact_fp8"
     emul, amb, _ = oracle.attention(path, case.q, case.k, case.v, dq, dk, case.dv)
     check_rows(gpu.reshape(-1, 128), emul.reshape(-1, 128), amb.reshape(-1), vmax_fp8(case))
+
+
+def test_nan_key_codes_per_path():
+    """A NaN code (0x7F) in a key row: Lean-P's saturating multiply-add turns
+    the NaN score into code 0 and the block maximum skips it, so that key gets
+    weight 0 and every output stays finite; the ablation's exponential
+    propagates the NaN to the rows that see the key (behaviour stated in
+    fp8attn.h)."""
+    case = wl.fp8_gaussian_case(1, 2, 2, 300, 128, 128, seeds=(82, 83, 84))
+    case.k[0, 100, :, 5] = 0x7F
+    q, k, v, d = dev_fp8(case)
+    lp = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d)
+    ab = fa.attn_fwd_ex(fa.ATTN_VARIANT_EXACT_FP8, q, k, v, *d)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(lp).all())
+    assert bool(torch.isfinite(ab[0, :100]).all()) and bool(torch.isnan(ab[0, 100:]).all())
