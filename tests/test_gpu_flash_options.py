@@ -114,3 +114,17 @@ def test_flash_attn_style_wrappers():
     ob = fa.flash_attn_bf16_func(qb, kb, vb, causal=True)
     torch.cuda.synchronize()
     assert torch.equal(ob, fa.attn_fwd_bf16(qb, kb, vb))
+
+
+@pytest.mark.parametrize("S", [1, 129, 511])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+def test_mla_gqa_batched_options(S, causal, variant):
+    """The MLA shape (Dqk 192, Dv 128) with GQA, B = 2, descales per (batch,
+    kv head) and the LSE, over ragged lengths, causal and not."""
+    B, Hq, Hkv = 2, 4, 2
+    case = wl.fp8_gaussian_case(B, Hq, Hkv, S, 192, 128, seeds=(118, 119, 120), outlier_seed=121,
+                                outliers_qk=4, factor=20.0, outliers_v=False)
+    rng = np.random.default_rng(122 + S)
+    dq, dk, dv = (x * rng.uniform(0.5, 2.0, (B, Hkv)) for x in (case.dq, case.dk, case.dv))
+    _fp8_parity(variant, case, dq, dk, dv, causal)
