@@ -2,7 +2,9 @@
 //
 // One persistent CTA per SM.  A work item is (batch b, query head h, query
 // block qb) with two 128-row query tiles (rows 256*qb .. 256*qb+255); the two
-// tiles share every K/V tile that TMA brings in.  Roles (12 warps):
+// tiles share every K/V tile that TMA brings in.  Items run longest first
+// (see decode_item for the chunked order of very large problems).  Roles (12
+// warps):
 //   warps 0-3   softmax of query tile 0 (thread = row)
 //   warps 4-7   softmax of query tile 1
 //   warp  8     TMA producer: Q tiles once per item, K/V tiles through a ring
@@ -21,17 +23,20 @@
 // softmax still works on the current one, and the P.V products are issued by
 // their own warp whenever a P_t(j) is ready.  The softmax of each tile thus
 // hides behind a whole period of tensor-core work (both tiles' QK and PV).
-// Two issuing warps matter on this hardware: a thread that issues tcgen05.mma
-// stalls on any later wait until its own MMAs drain, which idles the pipe
-// unless another thread is issuing.  This replaces the "two-wave ping-pong"
+// Two issuing warps: the QK products wait on S hand-overs and the P.V
+// products on P, and issuing four MMAs and a commit keeps a thread busy for
+// about 275 clocks (more under contention), so one thread serving both waits
+// would delay one product behind the other.  This replaces the "two-wave ping-pong"
 // of the MI355X design ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X",
 // "How does ZYFA work?"): asynchronous tcgen05 MMAs tracked by mbarriers
 // provide the overlap.
 //
 // Probability policies (softmax warpgroups):
-//   kLeanP     one multiply-add per probability rounded toward minus infinity
-//              into the magic range [2^23, 2^24), whose low byte is the e4m3
-//              code ("Lean P: one multiply-add instead of an exponential"); a
+//   kLeanP     one saturating multiply-add per probability rounded toward
+//              minus infinity, whose value floored to 1/128 is the e4m3 code,
+//              and packed floors that gather four codes per word (see
+//              leanp_codes4; "Lean P: one multiply-add instead of an
+//              exponential"); a
 //              power-of-two scale per 64-key block enters the P.V MMA as a
 //              UE8M0 block-scale factor, and the P.V product runs against
 //              [V | ones] so that column 128 of O accumulates the sum of the
