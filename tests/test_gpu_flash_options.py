@@ -128,3 +128,23 @@ def test_mla_gqa_batched_options(S, causal, variant):
     rng = np.random.default_rng(122 + S)
     dq, dk, dv = (x * rng.uniform(0.5, 2.0, (B, Hkv)) for x in (case.dq, case.dk, case.dv))
     _fp8_parity(variant, case, dq, dk, dv, causal)
+
+
+def test_float8_tensors_and_binding_errors():
+    """torch float8_e4m3fn tensors give the same bits as their uint8 views;
+    the binding refuses wrong dtypes, layouts and shapes before calling the
+    library."""
+    case = wl.fp8_gaussian_case(1, 4, 2, 200, 128, 128, seeds=(123, 124, 125))
+    q, k, v, d = _fp8_dev(case, case.dq, case.dk, case.dv)
+    a = fa.attn_fwd_fp8(q, k, v, *d)
+    b = fa.attn_fwd_fp8(*(t.view(torch.float8_e4m3fn) for t in (q, k, v)), *d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    with pytest.raises(TypeError):
+        fa.attn_fwd_fp8(q.float(), k, v, *d)                        # not e4m3 codes
+    with pytest.raises(ValueError):
+        fa.attn_fwd_fp8(q.transpose(1, 2), k, v, *d)                # not contiguous BSHD
+    with pytest.raises(TypeError):
+        fa.attn_fwd_fp8(q.cpu(), k, v, *d)                          # not on the GPU
+    with pytest.raises(fa.AttnError):
+        fa.attn_fwd_fp8(q[:, :, :3].contiguous(), k, v, *d)         # Hq % Hkv != 0
