@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3938462208,
-                    "sources_sha256": "b7e9a7bd6999dc6d5c73db5fd84aea4897766dca1e6c069d5a2194b8a3677f10"}
+PROFILED_TRAFFIC = {"bytes": 3945776384,
+                    "sources_sha256": "9157317641f4d6c3db153d29e39458480acd43f6659ae77853e58bc4e29b9eb3"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

@@ -120,6 +120,11 @@ struct Cfg {
   static constexpr int kPvSteps = kFp8 ? 4 : 8;         // 128 keys / (32 fp8 or 16 bf16)
   static constexpr int kPCols = kFp8 ? 32 : 64;         // TMEM columns of P per tile
   static constexpr int kPvN = kBlockScaled ? 144 : 128;  // P.V N (with the ones column)
+  // BF16: P.V of key tile j waits until the tile's S product of key tile j+1
+  // is issued (see pv_loop).  Measured on the FP8 paths, the same order was
+  // slower: there the P.V warp's issue-and-drain then delays P.V past the
+  // point where the softmax needs it.
+  static constexpr bool kOrderPv = !kFp8;
   // tensor-memory columns
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColP0 = 128, kColP1 = kFp8 ? 176 : 192;
@@ -196,6 +201,7 @@ struct __align__(8) Barriers {
   uint64_t s_drained[2];  // softmax t has copied S into registers
   uint64_t p_full[2];     // softmax t has written P_t(j)
   uint64_t o_done[2];     // PV_t(j) complete (PV commit)
+  uint64_t qk_go[2][2];   // S product n of tile t issued: qk_go[t][n % 2] (BF16)
   uint64_t o_free[2];     // softmax t has read O_t in its epilogue
   uint64_t drain[2];      // teardown: all MMAs of the QK / PV warp complete
   uint32_t tmem_base;
@@ -362,6 +368,8 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         if (stamp) FA8_TL(2 + t, j, 4);
         tc_fence_after();
         issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + st * C::kQkTileBytes);
+        // the P.V warp may now queue this tile's previous P.V product behind it
+        if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 1]);
         tc_commit(&bars.s_full[t]);
         if (stamp) FA8_TL(2 + t, j, 5);
         ++issued[t];
@@ -373,7 +381,17 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
   }
 }
 
-// PV warp: O_t += P_t V_j as soon as P_t(j) is written.
+// PV warp: O_t += P_t V_j as soon as P_t(j) is written.  With kOrderPv (BF16)
+// it also waits until S_t(j+1) has been issued, unless j is the tile's last key
+// tile: the tensor pipe runs products in issue order, so the S product, which
+// the other tile's softmax is about to wait for, does not queue behind a P.V
+// product that became ready at the same moment.  The QK warp arrives on
+// qk_go[t][n % 2] after issuing S product n of tile t, counted over all items,
+// and this warp consumes every arrival in order (at a tile's last key tile up
+// to S_t(j) itself, already issued), so it is never behind by more than the
+// arrival it waits for.  Two barriers per tile suffice: S_t(j+3) needs P_t(j+1),
+// which the softmax writes only after PV_t(j) is complete, so the QK warp is
+// never two phases ahead on either barrier.
 template <int V, int DQK>
 __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
   using C = Cfg<V, DQK>;
@@ -381,6 +399,8 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
   volatile int* ab = &bars.abort_flag;
   const uint64_t lim = p.wait_limit_ns;
   uint32_t kv_it = 0, p_cnt[2] = {0, 0}, items = 0;
+  uint32_t qk_base[2] = {0, 0};  // S products of each tile in earlier items
+  uint32_t go_seen[2] = {0, 0};  // qk_go arrivals consumed per tile
   for (int round = 0;; ++round) {
     const int idx = item_at(round, p.n_items);
     if (idx < 0) break;
@@ -400,6 +420,13 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
           // the previous item's epilogue must have read O_t
           if (!mbar_wait(&bars.o_free[t], (items & 1) ^ 1, ab, lim)) return;
         }
+        if constexpr (C::kOrderPv) {
+          const int nk = t ? nkv : nk0;
+          const uint32_t upto = qk_base[t] + (j + 1 < nk ? j + 1 : j);
+          for (; go_seen[t] <= upto; ++go_seen[t])
+            if (!mbar_wait(&bars.qk_go[t][go_seen[t] & 1], (go_seen[t] >> 1) & 1, ab, lim))
+              return;
+        }
         if (stamp) FA8_TL(2 + t, j, 1);
         tc_fence_after();
         issue_pv<V, DQK>(tmem, smem_base, t, C::kSmemV + st * C::kVTileBytes, j > 0);
@@ -408,6 +435,8 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
       }
       tc_commit(&bars.v_empty[st]);
     }
+    qk_base[0] += nk0;
+    qk_base[1] += nkv;
     ++items;
   }
 }
@@ -725,6 +754,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_drained[t], 128);
       mbar_init(&bars.p_full[t], 128);
       mbar_init(&bars.o_done[t], 1);
+      mbar_init(&bars.qk_go[t][0], 1);
+      mbar_init(&bars.qk_go[t][1], 1);
       mbar_init(&bars.o_free[t], 128);
       mbar_init(&bars.drain[t], 1);
     }
