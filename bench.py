@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3945776384,
-                    "sources_sha256": "9157317641f4d6c3db153d29e39458480acd43f6659ae77853e58bc4e29b9eb3"}
+PROFILED_TRAFFIC = {"bytes": 3941521408,
+                    "sources_sha256": "628af78baa5df992c29e1707bc5b09d611cb72c7f10e6fd7e966b98b34edda9d"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

@@ -201,7 +201,7 @@ struct __align__(8) Barriers {
   uint64_t s_drained[2];  // softmax t has copied S into registers
   uint64_t p_full[2];     // softmax t has written P_t(j)
   uint64_t o_done[2];     // PV_t(j) complete (PV commit)
-  uint64_t qk_go[2][2];   // S product n of tile t issued: qk_go[t][n % 2] (BF16)
+  uint64_t qk_go[2][4];   // S product n of tile t issued: qk_go[t][n % 4] (BF16)
   uint64_t o_free[2];     // softmax t has read O_t in its epilogue
   uint64_t drain[2];      // teardown: all MMAs of the QK / PV warp complete
   uint32_t tmem_base;
@@ -369,7 +369,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         tc_fence_after();
         issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + st * C::kQkTileBytes);
         // the P.V warp may now queue this tile's previous P.V product behind it
-        if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 1]);
+        if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 3]);
         tc_commit(&bars.s_full[t]);
         if (stamp) FA8_TL(2 + t, j, 5);
         ++issued[t];
@@ -386,12 +386,14 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
 // tile: the tensor pipe runs products in issue order, so the S product, which
 // the other tile's softmax is about to wait for, does not queue behind a P.V
 // product that became ready at the same moment.  The QK warp arrives on
-// qk_go[t][n % 2] after issuing S product n of tile t, counted over all items,
+// qk_go[t][n % 4] after issuing S product n of tile t, counted over all items,
 // and this warp consumes every arrival in order (at a tile's last key tile up
-// to S_t(j) itself, already issued), so it is never behind by more than the
-// arrival it waits for.  Two barriers per tile suffice: S_t(j+3) needs P_t(j+1),
-// which the softmax writes only after PV_t(j) is complete, so the QK warp is
-// never two phases ahead on either barrier.
+// to S_t(j) itself, already issued).  No barrier can run two phases ahead of
+// this warp: the next arrival on the barrier of n is n + 4, and S_t(n+4) is
+// issued only after the softmax has written P_t at a key tile two or more past
+// the P.V product that consumes n, which waits for that P.V product.  (With
+// two barriers this fails at an item's start, where P_t(0) is written without
+// waiting for any P.V product.)
 template <int V, int DQK>
 __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
   using C = Cfg<V, DQK>;
@@ -424,7 +426,7 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
           const int nk = t ? nkv : nk0;
           const uint32_t upto = qk_base[t] + (j + 1 < nk ? j + 1 : j);
           for (; go_seen[t] <= upto; ++go_seen[t])
-            if (!mbar_wait(&bars.qk_go[t][go_seen[t] & 1], (go_seen[t] >> 1) & 1, ab, lim))
+            if (!mbar_wait(&bars.qk_go[t][go_seen[t] & 3], (go_seen[t] >> 2) & 1, ab, lim))
               return;
         }
         if (stamp) FA8_TL(2 + t, j, 1);
@@ -754,8 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_drained[t], 128);
       mbar_init(&bars.p_full[t], 128);
       mbar_init(&bars.o_done[t], 1);
-      mbar_init(&bars.qk_go[t][0], 1);
-      mbar_init(&bars.qk_go[t][1], 1);
+      for (int i = 0; i < 4; ++i) mbar_init(&bars.qk_go[t][i], 1);
       mbar_init(&bars.o_free[t], 128);
       mbar_init(&bars.drain[t], 1);
     }
