@@ -194,7 +194,7 @@ def test_bitwise_identical_over_7200_launches():
 def test_every_variant_is_deterministic(variant, causal):
     """Every path, causal or not, with fp32 output and the log-sum-exp: 20
     launches on a multi-wave grid give the same bits (no atomics, a fixed
-    accumulation order)."""
+    accumulation order), and no launch reports a status."""
     if variant == fa.ATTN_VARIANT_BF16:
         b = wl.bf16_gaussian_case(2, 16, 4, 3000, 128, 128)
         args = dev_bf16(b)
@@ -202,12 +202,17 @@ def test_every_variant_is_deterministic(variant, causal):
         c = wl.fp8_gaussian_case(2, 16, 4, 3000, 128, 128, seeds=(67, 68, 69))
         q, k, v, d = dev_fp8(c)
         args = (q, k, v, *d)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     first = [t.clone() for t in fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32,
-                                                  causal=causal, return_lse=True)]
+                                                  causal=causal, return_lse=True,
+                                                  dev_status=status)]
     for _ in range(20):
         again = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
-                                 return_lse=True)
+                                 return_lse=True, dev_status=status)
         assert all(torch.equal(x, y) for x, y in zip(first, again))
+    torch.cuda.synchronize()
+    # a bounded wait that ran out would set ATTN_ERR_TIMEOUT and leave rows unwritten
+    assert int(status.item()) == fa.ATTN_OK, fa.status_string(int(status.item()))
 
 
 # ------------------------------------------------------------------ failure paths
