@@ -9,7 +9,8 @@
 //   warps 4-7   softmax of query tile 1
 //   warp  8     TMA producer: Q tiles once per item, K/V tiles through a ring
 //   warp  9     QK issuer: S = Q_t K_j^T for (j, t) = (0,0), (0,1), (1,0), ...
-//   warp  10    PV issuer: O_t += P_t V_j; owns tensor memory
+//   warp  10    PV issuer: O_t += P_t V_j; owns tensor memory (BF16: each
+//               P.V product is issued behind the tile's next S product)
 //   warp  11    idle (completes the last warpgroup)
 //
 // Tensor memory (512 columns x 128 lanes of 32-bit words), FP8 paths:
@@ -26,7 +27,8 @@
 // Two issuing warps: the QK products wait on S hand-overs and the P.V
 // products on P, and issuing four MMAs and a commit keeps a thread busy for
 // about 275 clocks (more under contention), so one thread serving both waits
-// would delay one product behind the other.  This replaces the "two-wave ping-pong"
+// would delay one product behind the other; its next wait would also stall
+// until its own MMAs drain.  This replaces the "two-wave ping-pong"
 // of the MI355X design ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X",
 // "How does ZYFA work?"): asynchronous tcgen05 MMAs tracked by mbarriers
 // provide the overlap.
