@@ -190,7 +190,12 @@ __global__ void __launch_bounds__(kQuantThreads) quant_codes_kernel(const void* 
   const int64_t ng = ((int64_t)gridDim.x * kQuantThreads) >> 5;
   const float a = *amax;
   const float sc = a > 0.0f ? 448.0f / a : 1.0f;
-  for (int64_t g = g0; g * kQuantVecPerWarp < n_vec; g += ng) {
+  const int64_t n_groups = (n_vec + kQuantVecPerWarp - 1) / kQuantVecPerWarp;
+  for (int64_t i = g0; i < n_groups; i += ng) {
+    // backwards: the amax pass swept forwards and has just left the end of x
+    // in L2, so the first groups read here are L2 hits (each code depends
+    // only on its vector and the amax, so the order changes no result)
+    const int64_t g = n_groups - 1 - i;
     const int64_t v = g * kQuantVecPerWarp + lane / kQuantLanes;
     float r[L::kPerLane];
     quant_load<D, F32>(x, v, n_vec, j, r);
