@@ -268,16 +268,18 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
     }
     if (*ab) break;
   }
-  if (*ab) {
-    // Before the CTA may exit, every copy this thread started must have landed.
-    constexpr uint64_t kDrainNs = 50000000ull;
-    volatile int dummy = 0;
-    for (uint32_t i = nk > (uint32_t)C::kStages ? nk - C::kStages : 0; i < nk; ++i)
-      mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
-    for (uint32_t i = nv > (uint32_t)C::kStages ? nv - C::kStages : 0; i < nv; ++i)
-      mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
-    if (q_it) mbar_wait(&bars.q_full, (q_it - 1) & 1, &dummy, kDrainNs);
-  }
+  // Before the CTA may exit, every copy this thread started must have landed:
+  // after an abort, and also after a normal end, since a wait in another role
+  // may still run out of time while the last loads are in flight.  Only the
+  // last kStages loads of K and of V can be in flight (a stage is reloaded
+  // only after its consumer has waited for the previous load).
+  constexpr uint64_t kDrainNs = 50000000ull;
+  volatile int dummy = 0;
+  for (uint32_t i = nk > (uint32_t)C::kStages ? nk - C::kStages : 0; i < nk; ++i)
+    mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
+  for (uint32_t i = nv > (uint32_t)C::kStages ? nv - C::kStages : 0; i < nv; ++i)
+    mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
+  if (q_it) mbar_wait(&bars.q_full, (q_it - 1) & 1, &dummy, kDrainNs);
 }
 
 // --------------------------------------------------------------------------

@@ -33,7 +33,20 @@ Data checks, at the moment each access happens:
 - the next item's first P.V product runs only after that read;
 - a ring stage or Q is reloaded only after every product that reads it ran.
 
-``run`` returns None, or a message for the first violation or deadlock.
+The failure path (``inject_timeout``): at a random moment one blocked wait
+runs out of time and sets the CTA's abort word, as the kernel's bounded waits
+do.
+- From then on a wait that would block returns instead, and its role leaves
+  its loop through the kernel's exit sequence.
+- The producer then waits for the loads it may still have in flight (the last
+  ``stages`` of K and of V, and the last Q).
+- Each issuing warp commits and waits for its own MMAs.
+
+At the CTA's exit, also after a normal run, no TMA load, MMA or commit
+arrival may still be in flight: each would write to the shared or tensor
+memory of the CTA that comes next.
+
+``run`` returns None, or raises ``Violation`` for the first violation or deadlock.
 """
 from __future__ import annotations
 
@@ -75,6 +88,10 @@ class Protocol:
     # planted mistakes, for the tests that show the checker finds them
     skip_drain_wait: bool = False
     skip_o_done_wait: bool = False
+    # the failure path: one bounded wait runs out of time
+    inject_timeout: bool = False
+    skip_producer_drain: bool = False
+    skip_mma_drain: bool = False
 
 
 @dataclass
@@ -113,7 +130,10 @@ class Model:
             **{f"o_done{t}": B(f"o_done{t}", 1) for t in range(2)},
             **{f"o_free{t}": B(f"o_free{t}", 1) for t in range(2)},
             **{f"qk_go{t}_{i}": B(f"qk_go{t}_{i}", 1) for t in range(2) for i in range(proto.qk_go)},
+            **{f"drain_{r}": B(f"drain_{r}", 1) for r in ("qk", "pv0", "pv1")},
         }
+        self.abort = False
+        self.n_k = self.n_v = self.n_q = 0  # loads the producer has issued
         self.st = _State()
         for t in range(2):
             self.st.p[t] = [None, True]
@@ -124,7 +144,7 @@ class Model:
         self.seq = 0
         self.last_issued = {}  # thread -> seq of its last issued MMA
         self.ran = -1        # seq of the last MMA run (the pipe is in order)
-        self.commits = []    # (thread, seq bound, barrier)
+        self.commits = []    # (thread, seq bound, barrier), in issue order
         self.tmas = []       # (barrier, kind, stage, version)
         self.roles = {"producer": self._producer(), "qk": self._qk()}
         if proto.split_pv:
@@ -158,7 +178,43 @@ class Model:
                         yield _wait(f"v_empty{w}_{st}", use - 1)
                 yield ("tma", f"v_full{st}", "V", st, (item, j))
                 kv_it += 1
+        # also after a normal end: a wait elsewhere may still run out of time
+        # while its last loads are in flight
+        yield from self._producer_drain()
         yield ("done",)
+
+    def _producer_drain(self):
+        """The kernel's producer before it leaves, after a normal end or an
+        abort: every copy it started must have landed before the CTA may
+        exit."""
+        if self.p.skip_producer_drain:
+            return
+        S = self.p.stages
+        for i in range(max(0, self.n_k - S), self.n_k):
+            yield ("wait_drain", f"k_full{i % S}", i // S)
+        for i in range(max(0, self.n_v - S), self.n_v):
+            yield ("wait_drain", f"v_full{i % S}", i // S)
+        if self.n_q:
+            yield ("wait_drain", "q_full", self.n_q - 1)
+
+    def _mma_drain(self, name):
+        """An issuing warp's last steps, after its loop ends or gives up: its
+        MMAs must be complete before tensor memory is released."""
+        if self.p.skip_mma_drain:
+            return
+        yield ("commit", name, f"drain_{name}")
+        yield ("wait_drain", f"drain_{name}", 0)
+
+    def _exit(self, name):
+        """The role's wait gave up (abort word set): leave its loop."""
+        def gen():
+            if name == "producer":
+                yield from self._producer_drain()
+            elif name in ("qk", "pv0", "pv1"):
+                yield from self._mma_drain(name)
+            yield ("done",)
+        self.roles[name] = gen()
+        self.next_op[name] = next(self.roles[name])
 
     def _qk(self):
         S = self.p.stages
@@ -182,6 +238,7 @@ class Model:
                 yield ("commit", "qk", f"k_empty{st}")
                 kv_it += 1
             yield ("commit", "qk", "q_empty")
+        yield from self._mma_drain("qk")
         yield ("done",)
 
     def _pv(self, w, tiles):
@@ -211,6 +268,7 @@ class Model:
                 kv_it += 1
             qk_base[0] += nk0
             qk_base[1] += nkv
+        yield from self._mma_drain(name)
         yield ("done",)
 
     def _softmax(self, t):
@@ -247,6 +305,12 @@ class Model:
 
     def _tma_issue(self, bar, kind, stage, version):
         st = self.st
+        if kind == "Q":
+            self.n_q += 1
+        elif kind == "K":
+            self.n_k += 1
+        else:
+            self.n_v += 1
         if kind == "Q":
             if st.q is not None and not self._all_read("Q", st.q):
                 raise Violation(f"Q reloaded for item {version} while products still read item {st.q}")
@@ -303,7 +367,7 @@ class Model:
             self.pipe.append((self.seq, op[1], op[2], op[3]))
             self.last_issued[op[1]] = self.seq
         elif kind == "commit":
-            self.commits.append((self.last_issued.get(op[1], -1), op[2]))
+            self.commits.append((op[1], self.last_issued.get(op[1], -1), op[2]))
         elif kind == "read_s":
             _, t, item, j = op
             if st.s_content != (t, item, j) or st.s_read:
@@ -337,39 +401,64 @@ class Model:
         """Random schedule: every role and every kind of asynchronous event
         gets a random speed for the whole run, so that schedules where one
         role lags far behind the others (the ones that expose aliasing) come
-        up often."""
+        up often.  With ``inject_timeout`` one blocked wait gives up at a
+        random step."""
         speed = {name: self.rng.choice((0.02, 0.2, 1.0)) for name in self.roles}
         for kind in ("pipe", "commit", "tma"):
             speed[kind] = self.rng.choice((0.05, 0.3, 1.0))
+        timeout_at = self.rng.randint(0, 600) if self.p.inject_timeout else None
         done = set()
-        for _ in range(max_steps):
-            choices = []
-            for name, op in self.next_op.items():
+        for step in range(max_steps):
+            choices, blocked = [], []
+            for name in list(self.next_op):
+                op = self.next_op[name]
                 if name in done:
                     continue
                 if op[0] == "done":
                     done.add(name)
                     continue
-                if op[0] == "wait" and not self._wait_state(op):
+                if op[0] in ("wait", "wait_drain") and not self._wait_state(op):
+                    if op[0] == "wait" and self.abort:
+                        self._exit(name)  # the bounded wait sees the abort word
+                        choices.append(("none", name))
+                    elif op[0] == "wait":
+                        blocked.append(name)
                     continue
                 choices.append(("role", name))
+            if len(done) == len(self.roles):
+                # every role has finished: the CTA exits now
+                if self.tmas:
+                    raise Violation(f"the CTA exits with TMA loads in flight: {self.tmas}")
+                if self.pipe:
+                    raise Violation(f"the CTA exits with MMAs in flight: {self.pipe}")
+                if self.commits:
+                    raise Violation(f"the CTA exits with commit arrivals pending: {self.commits}")
+                return None
+            if timeout_at is not None and step >= timeout_at and blocked:
+                # this wait's time limit runs out: it sets the abort word
+                self.abort = True
+                self._exit(self.rng.choice(blocked))
+                timeout_at = None
+                continue
             if self.pipe:
                 choices.append(("pipe", None))
-            for i, (bound, _) in enumerate(self.commits):
-                if bound <= self.ran:
+            for i, (thread, bound, _) in enumerate(self.commits):
+                # a thread's commits arrive in order, each once its MMAs ran
+                if bound <= self.ran and all(c[0] != thread for c in self.commits[:i]):
                     choices.append(("commit", i))
             for i in range(len(self.tmas)):
                 choices.append(("tma", i))
             if not choices:
-                if len(done) == len(self.roles):
-                    return None
                 stuck = {n: op for n, op in self.next_op.items() if n not in done}
                 raise Violation(f"deadlock: {stuck}")
-            weights = [speed[arg] if what == "role" else speed[what] for what, arg in choices]
+            weights = [speed.get(arg, 1.0) if what in ("role", "none") else speed[what]
+                       for what, arg in choices]
             what, arg = self.rng.choices(choices, weights)[0]
+            if what == "none":
+                continue
             if what == "role":
                 op = self.next_op[arg]
-                if op[0] != "wait":
+                if op[0] not in ("wait", "wait_drain"):
                     self._role_op(arg, op)
                 self.next_op[arg] = next(self.roles[arg])
             elif what == "pipe":
@@ -377,7 +466,7 @@ class Model:
                 self._run_mma(thread, kind, args)
                 self.ran = seq
             elif what == "commit":
-                _, bar = self.commits.pop(arg)
+                _, _, bar = self.commits.pop(arg)
                 self.bars[bar].arrive()
             else:
                 self.bars[self.tmas.pop(arg)].arrive()

@@ -8,6 +8,10 @@ schedules with random per-role speeds.
 - Mistakes planted in the model are found: two ``qk_go`` barriers per tile
   alias (a first GPU build of that variant ended some launches on the bounded
   wait's timeout), and dropping the S-drain or P.V-done wait is an overwrite.
+- The failure path: with one bounded wait running out of time at a random
+  moment, every role leaves and the CTA exits with no TMA load, MMA or commit
+  arrival in flight; without the producer's or an issuing warp's drain it
+  does not.
 """
 import os
 import sys
@@ -63,3 +67,23 @@ def test_model_reports_a_deadlock():
     m.bars["q_full"].pending = 2
     with pytest.raises(sm.Violation, match="deadlock"):
         m.run()
+
+
+@pytest.mark.parametrize("proto", [
+    sm.Protocol(stages=4, inject_timeout=True),
+    sm.Protocol(stages=3, inject_timeout=True),
+    sm.Protocol(stages=2, order_pv=True, inject_timeout=True),
+], ids=["fp8", "fp8_mla", "bf16"])
+def test_a_timed_out_wait_leaves_nothing_in_flight(proto):
+    assert sm.check(proto, range(600)) is None
+
+
+def test_producer_without_drain_can_exit_with_loads_in_flight():
+    found = sm.check(sm.Protocol(inject_timeout=True, skip_producer_drain=True), range(600))
+    assert found is not None and "TMA loads in flight" in found[2], found
+
+
+def test_issuing_warps_without_drain_exit_with_mmas_in_flight():
+    found = sm.check(sm.Protocol(inject_timeout=True, skip_mma_drain=True), range(600))
+    assert found is not None and ("MMAs in flight" in found[2]
+                                  or "commit arrivals pending" in found[2]), found
