@@ -119,9 +119,45 @@ def load_peaks():
             d = json.load(f)
         return {"bf16_burst": float(d["bf16_tflops"]),
                 "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured",
+                "sustained_mhz": (d.get("clocks_under_load") or {}).get("sm_mhz_median")}
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0,
-            "source": "fallback"}
+            "source": "fallback", "sustained_mhz": None}
+
+
+# Tensor-pipe work per SM and clock, measured on GB300 with one-CTA
+# microbenchmarks: a 128x128x32 FP8 MMA (kind::f8f6f4, also block-scaled)
+# every 64 clocks, a 128x128x16 BF16 MMA every 64 clocks.  Times the SM count
+# and a clock, this is the clock-rated ceiling of a contraction.
+MMA_FLOP_PER_CLK_SM = {"fp8": 16384.0, "bf16": 8192.0}
+
+
+def clock_rated_peak(kind, sms, mhz):
+    """TFLOP/s the tensor pipes of `sms` SMs issue at `mhz` (None if unknown)."""
+    if not mhz:
+        return None
+    return MMA_FLOP_PER_CLK_SM[kind] * sms * mhz * 1e6 / 1e12
+
+
+def clock_normalised(achieved, kind, peaks, sms, kernel_mhz):
+    """The achieved rate against two clock-aware denominators: the measured
+    sustained bf16 GEMM scaled from the clock it ran at to the kernel's
+    median clock (x2 for FP8, the nominal ratio), and the tensor pipes'
+    clock-rated ceiling at the kernel's median clock."""
+    out = {"kernel_sm_mhz": kernel_mhz}
+    if kernel_mhz and peaks.get("sustained_mhz"):
+        ratio = FP8_OVER_BF16 if kind == "fp8" else 1.0
+        p = peaks["bf16_sustained"] * ratio * kernel_mhz / peaks["sustained_mhz"]
+        out["measured_sustained_at_kernel_clock"] = {
+            "peak": p, "frac": achieved / p,
+            "how": (f"{peaks['bf16_sustained']} TFLOP/s bf16 sustained at a median "
+                    f"{peaks['sustained_mhz']} MHz, x {ratio} x (kernel MHz / that MHz)")}
+    p = clock_rated_peak(kind, sms, kernel_mhz)
+    if p:
+        out["mma_issue_rate_at_kernel_clock"] = {
+            "peak": p, "frac": achieved / p,
+            "how": f"{MMA_FLOP_PER_CLK_SM[kind]:.0f} FLOP/clk/SM x {sms} SMs x kernel MHz"}
+    return out
 
 
 # --------------------------------------------------------------------------- energy
@@ -418,6 +454,20 @@ def run_ours(args, rank, world, local_rank):
     def step_abl():
         fa.attn_fwd_fp8_exact(q, k, v, *d, out=out)
     ms_abl = timed(step_abl, max(3, args.steps // 4), 3)
+    # the diagnostic block-exact variant (Lean-P with an exponential for the
+    # code), same workload: splits Lean-P's gain into its two steps
+    def step_bx():
+        fa.attn_fwd_ex(fa.ATTN_VARIANT_BLOCK_EXACT, q, k, v, *d, out=out,
+                       out_dtype=fa.ATTN_OUT_BF16)
+    ms_bx = timed(step_bx, max(3, args.steps // 4), 3)
+    # sustained: back-to-back Lean-P calls for about args.sustained_s seconds,
+    # with the SM clock sampled throughout
+    n_sus = max(10, int(args.sustained_s * 1e3 / max(ms, 1e-3)))
+    clk_sus = ClockSampler(uuid)
+    clk_sus.start()
+    time.sleep(0.3)
+    ms_sus = timed(step, n_sus, 0)
+    clk_sus = clk_sus.stop()
 
     # end to end through the public API with host buffers: every step copies
     # its q, k, v from pinned memory and its output back into pinned memory.
@@ -439,11 +489,16 @@ def run_ours(args, rank, world, local_rank):
     # download is complete.
     e2e = E2EPipeline(torch, fa, dev, (hq, hk, hv), d, hout, stream)
     ms_e2e = e2e.timed(n_e2e, 4, barrier)
-    del e2e
     h2d = hq.numel() + hk.numel() + hv.numel()
     d2h = hout.numel() * 2
-
+    del e2e, hq, hk, hv, hout
     peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # the second target and the other shapes, each timed alone on its own
+    # workload: BF16 at 16K (GQA 32/8) and Lean-P at the MLA shape
+    extra = {} if args.no_extra else extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms,
+                                                max(5, args.steps // 4))
+
     peak_fp8 = peaks["bf16_burst"] * FP8_OVER_BF16
     per_gpu = F / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": job_tflops(F, world, ms), "unit": "TFLOP/s",
@@ -457,7 +512,18 @@ def run_ours(args, rank, world, local_rank):
                        "flop_count": "causal 2*B*Hq*(Dqk+Dv)*S*(S+1)/2 per rank"},
             "value_square_formula": job_tflops(Fsq, world, ms),
             "frac_of_fp8_peak": per_gpu / peak_fp8,
+            "frac_clock_aware": clock_normalised(per_gpu, "fp8", peaks, sms, clk.get("sm_mhz")),
             "ablation_exact_fp8": {"value": job_tflops(F, world, ms_abl), "ms_per_step": ms_abl},
+            "block_exact_fp8": {"value": job_tflops(F, world, ms_bx), "ms_per_step": ms_bx,
+                                "note": "Lean-P's block scale and rounded row sum with an "
+                                        "exponential in place of the one-FMA code"},
+            "sustained": {"value": job_tflops(F, world, ms_sus), "ms_per_step": ms_sus,
+                          "calls": n_sus, "seconds": n_sus * ms_sus / 1e3, "clocks": clk_sus,
+                          "tflops_per_ghz": (per_gpu * ms / ms_sus) / (clk_sus["sm_mhz"] / 1e3)
+                          if clk_sus.get("sm_mhz") else None,
+                          "frac_clock_aware": clock_normalised(F / (ms_sus * 1e-3) / 1e12, "fp8",
+                                                               peaks, sms, clk_sus.get("sm_mhz"))},
+            **extra,
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak_fp8,
                          "unit": "TFLOP/s", "frac": per_gpu / peak_fp8,
                          "traffic": args.traffic if args.traffic is not None else profiled_traffic(),
@@ -501,6 +567,54 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms, n):
+    """BF16 exact softmax on bf16_gqa_h32_8_s16k_d128 and Lean-P on the MLA
+    shape (fp8_mla_h16_s32k_dqk192_dv128_outliers), each timed on its own
+    inputs (larger than L2) with the clock sampled."""
+    legs = {}
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    for key, name in (("bf16_c3", "bf16_gqa_h32_8_s16k_d128"),
+                      ("leanp_mla_c5", "fp8_mla_h16_s32k_dqk192_dv128_outliers")):
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        F = causal_flops(B, Hq, S, Dqk, Dv)
+        o = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+        if key == "bf16_c3":
+            q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                       for a in (case.q, case.k, case.v))
+            fn, kind = (lambda: fa.attn_fwd_bf16(q, k, v, out=o)), "bf16"
+            peak = peaks["bf16_burst"]
+        else:
+            q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+            d = [torch.tensor([x], dtype=torch.float32, device=dev)
+                 for x in (case.dq, case.dk, case.dv)]
+            fn, kind = (lambda: fa.attn_fwd_fp8(q, k, v, *d, out=o)), "fp8"
+            peak = peaks["bf16_burst"] * FP8_OVER_BF16
+        clk = ClockSampler(uuid)
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        clk.start()
+        time.sleep(0.3)
+        ms = timed(fn, n, 0)
+        clk = clk.stop()
+        tf = F / (ms * 1e-3) / 1e12
+        legs[key] = {"workload": name, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
+                     "steps": n, "peak": peak, "frac": tf / peak,
+                     "peak_note": f"{peaks['source']} bf16 burst"
+                                  + (f" x {FP8_OVER_BF16}" if kind == "fp8" else ""),
+                     "frac_clock_aware": clock_normalised(tf, kind, peaks, sms,
+                                                          clk.get("sm_mhz")),
+                     "clocks": clk}
+        del q, k, v, o
+        torch.cuda.empty_cache()
+    return legs
 
 
 # --only PATH: the workload each path is profiled on (headline FP8 shape, the
@@ -832,6 +946,10 @@ def main():
     ap.add_argument("--ref-row-budget", type=int, default=8192,
                     help="oracle rows over the whole reference run")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the BF16 and MLA legs of the bench line")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back calls for the sustained leg")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the same kernel")
     ap.add_argument("--workload", default=WORKLOAD, help="configuration name (profiling)")

@@ -318,19 +318,34 @@ def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=No
     return (out, lse) if return_lse else out
 
 
+def host_descale(name, x):
+    """A descale given as a host number: it must be finite and greater than
+    zero (the library's contract; device descales cannot be checked without
+    a synchronisation).  Returns it as a float."""
+    try:
+        f = float(x)
+    except (TypeError, ValueError):
+        raise TypeError(f"{name} must be a number or a float32 CUDA tensor") from None
+    if not (f > 0.0 and f != float("inf")):
+        raise ValueError(f"{name} must be finite and greater than zero, got {x!r}")
+    return f
+
+
 def flash_attn_fp8_func(q, k, v, q_descale=None, k_descale=None, v_descale=None,
                         softmax_scale=None, causal=True, return_softmax_lse=False, exact=False):
     """flash_attn_func-style call on e4m3 inputs (uint8 codes, BSHD): the
     Lean-P path, or the exact-softmax ablation with ``exact=True``.
-    Descales default to 1; they may be [B, Hkv] tensors."""
-    one = None
-    if q_descale is None or k_descale is None or v_descale is None:
-        one = torch.ones(1, dtype=torch.float32, device=q.device)
+    Descales default to 1; each may be a one-element or [B, Hkv] float32 CUDA
+    tensor, or a host number (checked: finite and greater than zero)."""
+    def dev(name, x):
+        if x is None:
+            x = 1.0
+        if isinstance(x, torch.Tensor):
+            return x
+        return torch.tensor([host_descale(name, x)], dtype=torch.float32, device=q.device)
     return attn_fwd_full(ATTN_VARIANT_EXACT_FP8 if exact else ATTN_VARIANT_LEANP, q, k, v,
-                         one if q_descale is None else q_descale,
-                         one if k_descale is None else k_descale,
-                         one if v_descale is None else v_descale,
-                         causal=causal, softmax_scale=softmax_scale,
+                         dev("q_descale", q_descale), dev("k_descale", k_descale),
+                         dev("v_descale", v_descale), causal=causal, softmax_scale=softmax_scale,
                          return_lse=return_softmax_lse)
 
 

@@ -273,13 +273,16 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
   // may still run out of time while the last loads are in flight.  Only the
   // last kStages loads of K and of V can be in flight (a stage is reloaded
   // only after its consumer has waited for the previous load).
+  // A drain that runs out of time is reported like any other expired wait.
   constexpr uint64_t kDrainNs = 50000000ull;
-  volatile int dummy = 0;
+  volatile int gave_up = 0;
+  bool ok = true;
   for (uint32_t i = nk > (uint32_t)C::kStages ? nk - C::kStages : 0; i < nk; ++i)
-    mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
+    ok &= mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &gave_up, kDrainNs);
   for (uint32_t i = nv > (uint32_t)C::kStages ? nv - C::kStages : 0; i < nv; ++i)
-    mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &dummy, kDrainNs);
-  if (q_it) mbar_wait(&bars.q_full, (q_it - 1) & 1, &dummy, kDrainNs);
+    ok &= mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &gave_up, kDrainNs);
+  if (q_it) ok &= mbar_wait(&bars.q_full, (q_it - 1) & 1, &gave_up, kDrainNs);
+  if (!ok) *ab = 1;
 }
 
 // --------------------------------------------------------------------------
@@ -805,15 +808,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       pv_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
     if (lane_id() == 0) {
-      // every MMA this thread issued must be complete before TMEM is released
-      volatile int dummy = 0;
+      // every MMA this thread issued must be complete before TMEM is released;
+      // a drain that runs out of time is reported like any other expired wait
+      volatile int gave_up = 0;
       tc_commit(&bars.drain[role]);
-      mbar_wait(&bars.drain[role], 0, &dummy, 50000000ull);
+      if (!mbar_wait(&bars.drain[role], 0, &gave_up, 50000000ull))
+        *reinterpret_cast<volatile int*>(&bars.abort_flag) = 1;
     }
     __syncwarp();
   }
 
-  // Teardown (the producer has already waited for its copies if a role gave up).
+  // Teardown: the producer has waited for its last copies (on every exit) and
+  // each MMA warp for its MMAs; an expired wait anywhere sets the status word.
   tc_fence_before();
   __syncthreads();
   if (bars.abort_flag && threadIdx.x == 0 && p.status) atomicExch(p.status, 5);

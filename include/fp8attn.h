@@ -41,6 +41,13 @@
  * DEVICE memory (per-tensor descales), so a call can be captured in a CUDA
  * graph.  BF16 inputs are bf16 values.
  *
+ * Descales must be finite and greater than zero (a descale is amax/448 of
+ * the tensor, 1 for an all-zero tensor).  They live on the device, so the
+ * library cannot check them: with a zero, negative or non-finite descale the
+ * kernels still run to completion without a fault, but the output (and the
+ * LSE) is unspecified.  The Python binding rejects such values where it sees
+ * them on the host.
+ *
  * Non-finite codes: e4m3 has no infinities; a NaN code (0x7F, 0xFF) in q or k
  * makes that score NaN.  The Lean-P path gives such a key weight 0 (its
  * saturating multiply-add flushes NaN to 0 and the block maximum skips it);

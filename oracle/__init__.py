@@ -93,8 +93,9 @@ def _load():
         lib.oracle_emul_variant_e.argtypes = [vp, vp, vp, dp, dp, dp, ctypes.c_int, ctypes.c_int,
                                               *shape, ctypes.c_double, i64p, ctypes.c_int64,
                                               ctypes.c_double, dp, dp, dp]
+        lib.oracle_emul_leanp_a3.argtypes = lib.oracle_emul_variant_e.argtypes
         for fn in ("oracle_ref_fp64_ex", "oracle_emul_leanp_ex", "oracle_emul_exact_ex",
-                   "oracle_emul_variant_e"):
+                   "oracle_emul_variant_e", "oracle_emul_leanp_a3"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.oracle_quantize_e4m3.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
@@ -356,6 +357,9 @@ def attention(path, q, k, v, dq=1.0, dk=1.0, dv=1.0, scale=None, rows=None, caus
         rc = lib.oracle_ref_fp64_ex(_ptr(q), _ptr(k), _ptr(v), int(bf16), *args, _dptr(out), _dptr(lse))
     elif path == "leanp":
         rc = lib.oracle_emul_leanp_ex(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
+                                      _dptr(amb), _dptr(lse))
+    elif path == "leanp_a3":
+        rc = lib.oracle_emul_leanp_a3(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),
                                       _dptr(amb), _dptr(lse))
     elif path == "variant_e":
         rc = lib.oracle_emul_variant_e(_ptr(q), _ptr(k), _ptr(v), *args, float(kappa), _dptr(out),

@@ -27,6 +27,9 @@
  *                           (the "hardware exponential" column of [ART-MTP]
  *                           "How does ZYFA compare with other attention kernels?").
  *   oracle_emul_bf16     -- the exact-softmax BF16 path ([ART-MTP] "TL;DR").
+ *   oracle_emul_leanp_a3 -- O-2 under the second reading of the block scale:
+ *                           the code grid anchored at the running row maximum
+ *                           instead of at integer log2 values.
  *   The *_ex forms take the options of a flash_attn_func-style call ([ART-MTP]
  *   "TL;DR" names that interface): causal or not, descales per (batch, kv
  *   head) or per tensor, and a per-row log-sum-exp of the path's own row sum.
@@ -45,6 +48,8 @@
  *     order in which key blocks are visited.
  *   - the exact FP8 ablation and the BF16 path use a running max updated once
  *     per 128-key tile in ascending key order.
+ *   - descales are finite and positive (amax/448 of a tensor, or 1); every
+ *     definition rejects other values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -134,6 +139,17 @@ static double dsc(const double *a, const opts_t *o, const shape_t *sh, int b, in
   return a[(int64_t)b * sh->Hkv + g];
 }
 
+/* The descales must be finite and positive: a descale is amax/448 of a
+ * tensor (1 for an all-zero one), and the library takes the same contract. */
+static int descales_valid(const opts_t *o, const shape_t *sh) {
+  const int64_t n = o->per_bkv ? (int64_t)sh->B * sh->Hkv : 1;
+  for (int64_t t = 0; t < n; ++t) {
+    const double a = o->dq[t], b = o->dk[t], c = o->dv[t];
+    if (!(isfinite(a) && a > 0.0 && isfinite(b) && b > 0.0 && isfinite(c) && c > 0.0)) return 0;
+  }
+  return 1;
+}
+
 /* Number of keys row i attends to. */
 static int keys_of(const opts_t *o, const shape_t *sh, int i) { return o->causal ? i + 1 : sh->S; }
 
@@ -211,6 +227,7 @@ static int ref_fp64_impl(const void *q, const void *k, const void *v, int is_bf1
                          shape_t sh, double scale, const int64_t *rows, int64_t nrows,
                          double *out, double *lse) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
+  if (!descales_valid(&o, &sh)) return ORACLE_BAD_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;
@@ -316,6 +333,7 @@ static int leanp_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts
                       double scale, const int64_t *rows, int64_t nrows, double kappa, double *out,
                       double *amb, double *lse, int exact_p) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
+  if (!descales_valid(&o, &sh)) return ORACLE_BAD_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;
@@ -449,6 +467,120 @@ int oracle_emul_variant_e(const uint8_t *q, const uint8_t *k, const uint8_t *v, 
 }
 
 /* ---------------------------------------------------------------------------
+ * O-2, second reading: Lean-P codes anchored at the row's running maximum.
+ *
+ * The same two passages as O-2 ([ART-MTP] "Lean P: one multiply-add instead of
+ * an exponential", "Per-block scaling and a rounded row sum") leave open what
+ * the power of two of a block is relative to.  O-2 anchors the code grid at
+ * integer log2 values; this reading anchors it at the running row maximum m,
+ * so that the key holding the maximum gets exactly the code of 2^T.  With
+ * lambda = log2(e)*scale*dq*dk, T = 7, C = 56 + 8T = 112 and eps = 2^-6, per
+ * row, for each 128-key tile in ascending order (keys j <= i, or all j < S):
+ *   m_new = max(m, max_j s_j);  if m_new > m:  O, l *= 2^(lambda*(m - m_new))
+ *           (0 when m = -inf), m = m_new
+ *   for each 64-key block beta of the tile that holds an unmasked key:
+ *     k   = floor(lambda * (m - max_{j in beta} s_j))             (integer >= 0)
+ *     c_j = clamp(floor(8*lambda*(s_j - m) + 8k + C + eps), 0, 126)
+ *     O  += 2^(-T-k) * sum_j dec(c_j) * v_j;   l += 2^(-T-k) * sum_j dec(c_j)
+ *   out = dv * O / l;   lse = ln l + lambda * m * ln 2.
+ * amb: as for O-2, with every code's band widened by twice the band of the
+ * running maximum (its fp32 value shifts every code of the row), and the
+ * block's k taken both ways when lambda*(m - block max) is within the band of
+ * an integer.
+ * ------------------------------------------------------------------------- */
+#define LEANP_A3_EPS (1.0 / 64.0)
+
+static double a3_weight(double u, double um, int k) {
+  return oracle_e4m3_decode((unsigned)leanp_code(u - um + 8.0 * k + LEANP_C + LEANP_A3_EPS)) *
+         ldexp(1.0, -LEANP_T - k);
+}
+
+static int leanp_a3_impl(const uint8_t *q, const uint8_t *k, const uint8_t *v, opts_t o,
+                         shape_t sh, double scale, const int64_t *rows, int64_t nrows,
+                         double kappa, double *out, double *amb, double *lse) {
+  if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < nrows; ++r) {
+    int b, h, i;
+    row_at(&sh, rows, r, &b, &h, &i);
+    const double lam = scale * dsc(o.dq, &o, &sh, b, h) * dsc(o.dk, &o, &sh, b, h) / log(2.0);
+    const double dv = dsc(o.dv, &o, &sh, b, h);
+    const int n = keys_of(&o, &sh, i);
+    double *u = (double *)malloc(sizeof(double) * (size_t)n); /* 8*lambda*s_j, code units */
+    double *du = (double *)malloc(sizeof(double) * (size_t)n);
+    double *O = (double *)calloc((size_t)sh.Dv, sizeof(double));
+    for (int j = 0; j < n; ++j) {
+      double s, a;
+      dot_row(q, k, &sh, 0, b, h, i, j, &s, &a);
+      u[j] = 8.0 * lam * s;
+      du[j] = kappa * 8.0 * fabs(lam) * a + fabs(u[j]) * ldexp(1.0, -21);
+    }
+    double um = -INFINITY, dum = 0.0, l = 0.0, dmass = 0.0;
+    for (int t0 = 0; t0 < n; t0 += TILE_KEYS) {
+      const int t1 = t0 + TILE_KEYS < n ? t0 + TILE_KEYS : n;
+      double ut = -INFINITY, dut = 0.0;
+      for (int j = t0; j < t1; ++j)
+        if (u[j] > ut) { ut = u[j]; dut = du[j]; }
+      if (ut > um) {
+        const double alpha = um == -INFINITY ? 0.0 : exp2((um - ut) / 8.0);
+        for (int d = 0; d < sh.Dv; ++d) O[d] *= alpha;
+        l *= alpha;
+        dmass *= alpha;
+        um = ut;
+        dum = dut;
+      }
+      for (int j0 = t0; j0 < t1; j0 += LEANP_BLOCK) {
+        const int j1 = j0 + LEANP_BLOCK < t1 ? j0 + LEANP_BLOCK : t1;
+        double bmax = -INFINITY, dbm = 0.0;
+        for (int j = j0; j < j1; ++j)
+          if (u[j] > bmax) { bmax = u[j]; dbm = du[j]; }
+        const double y = (um - bmax) / 8.0; /* lambda * (m - block max) */
+        const int kb = (int)floor(y);
+        for (int j = j0; j < j1; ++j) {
+          const double w = a3_weight(u[j], um, kb);
+          l += w;
+          for (int d = 0; d < sh.Dv; ++d) O[d] += w * v_val(v, &sh, 0, b, h, j, d);
+          if (amb) {
+            const double x = u[j] - um + 8.0 * kb + LEANP_C + LEANP_A3_EPS;
+            const double nr = floor(x + 0.5);
+            if (fabs(x - nr) < du[j] + 2.0 * dum) {
+              const double f = ldexp(1.0, -LEANP_T - kb);
+              dmass += fabs(oracle_e4m3_decode((unsigned)leanp_code(nr + 0.5)) -
+                            oracle_e4m3_decode((unsigned)leanp_code(nr - 0.5))) * f;
+            }
+          }
+        }
+        if (amb) {
+          const double ny = floor(y + 0.5);
+          if (ny >= 1.0 && fabs(y - ny) < (dbm + dum) / 8.0) /* k may be ny - 1 or ny */
+            for (int j = j0; j < j1; ++j)
+              dmass += fabs(a3_weight(u[j], um, (int)ny) - a3_weight(u[j], um, (int)ny - 1));
+        }
+      }
+    }
+    for (int d = 0; d < sh.Dv; ++d) out[r * sh.Dv + d] = dv * O[d] / l;
+    if (amb) amb[r] = dmass / l;
+    if (lse) lse[r] = log(l) + um / 8.0 * log(2.0);
+    free(u);
+    free(du);
+    free(O);
+  }
+  return ORACLE_OK;
+}
+
+int oracle_emul_leanp_a3(const uint8_t *q, const uint8_t *k, const uint8_t *v, const double *dq,
+                         const double *dk, const double *dv, int per_bkv, int causal, int B,
+                         int Hq, int Hkv, int S, int Dqk, int Dv, double scale,
+                         const int64_t *rows, int64_t nrows, double kappa, double *out,
+                         double *amb, double *lse) {
+  shape_t sh = {B, Hq, Hkv, S, Dqk, Dv};
+  if (!dq || !dk || !dv) return ORACLE_BAD_ARG;
+  opts_t o = {dq, dk, dv, per_bkv, causal};
+  if (!descales_valid(&o, &sh)) return ORACLE_BAD_ARG;
+  return leanp_a3_impl(q, k, v, o, sh, scale, rows, nrows, kappa, out, amb, lse);
+}
+
+/* ---------------------------------------------------------------------------
  * O-3 / O-4: exact-softmax paths with a running max (128-key tiles, ascending).
  *
  * For each tile t (keys 128t .. 128t+127, j <= i):
@@ -465,6 +597,7 @@ static int exact_impl(const void *q, const void *k, const void *v, int is_bf16, 
                       shape_t sh, double scale, const int64_t *rows, int64_t nrows, double kappa,
                       double *out, double *amb, double *lse) {
   if (check_shape(&sh) || rows_valid(&sh, rows, nrows)) return ORACLE_BAD_ARG;
+  if (!descales_valid(&o, &sh)) return ORACLE_BAD_ARG;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < nrows; ++r) {
     int b, h, i;

@@ -120,3 +120,16 @@ def test_release_library_has_no_timeline(lib):
     import numpy as np
     buf = np.zeros(16, dtype=np.uint64)
     assert lib.attn_debug_timeline(buf.ctypes.data, buf.size, 1) == fa.ATTN_ERR_UNSUPPORTED
+
+
+def test_host_descales_must_be_finite_and_positive():
+    """The binding checks descales it is given as host numbers (the library's
+    contract: finite and greater than zero); device descales cannot be read
+    without a synchronisation and are the caller's responsibility."""
+    assert fa.host_descale("q_descale", 0.0125) == 0.0125
+    assert fa.host_descale("q_descale", 3) == 3.0
+    for bad in (0.0, -0.5, float("inf"), float("-inf"), float("nan")):
+        with pytest.raises(ValueError):
+            fa.host_descale("k_descale", bad)
+    with pytest.raises(TypeError):
+        fa.host_descale("v_descale", "one")

@@ -1,16 +1,20 @@
 """GPU parity at the full sizes of the measured workloads, on sampled rows.
 
 Every configuration runs the kernel exactly as the benchmark launches it
-(whole problem, persistent grid).  The oracle then recomputes a sample of
-rows one by one: tile edges, the first and last rows, the longest prefixes
-and random rows of every head.  Gates:
-- Against the CPU emulation of the identical scheme: max-abs error per row
-  <= 2e-3 * max|v~| (plus the oracle's rounding-ambiguity term).
-- Against fp64 attention, relative RMS: <= 3e-2 for FP8 where the scheme
-  itself meets it, and <= 5e-3 for BF16.  On the diffuse Gaussian 32K
-  workload the scheme's own error is about 3.2e-2, and the emulation shows
-  the same.  There the GPU error must equal the emulation's within 3 %, and
-  both must stay below 3.5e-2.
+(whole problem, persistent grid).  The oracle then recomputes two samples of
+rows one by one: tile edges, the first and last rows and the middle of three
+heads (edge rows), and rows drawn uniformly over every (batch, head, row)
+(random rows).  Gates:
+- Against the CPU emulation of the identical scheme, on every sampled row:
+  max-abs error per row <= 2e-3 * max|v~| (plus the oracle's rounding-
+  ambiguity term, which at most 1% of the rows may need).
+- Against fp64 attention, relative RMS over the random rows (the edge rows
+  are mostly short prefixes whose large outputs would dominate a pooled
+  figure): <= 3e-2 for FP8, <= 5e-3 for BF16.  The emulation's own figure on
+  the same rows is computed beside it, and the GPU's must equal it within 3%.
+  On the diffuse Gaussian 32K workload the integer-binade Lean-P scheme sits
+  above 3e-2 by itself (the CPU pin test_oracle_scheme_floor.py shows why);
+  that gate is an expected failure, kept strict so that it reports a change.
 - The ratio of Lean-P error to the exact-softmax FP8 ablation error is
   reported, not gated.
 """
@@ -22,11 +26,12 @@ import fp8_causal_prefill_flash_gb300 as fa
 import oracle
 from fp8_causal_prefill_flash_gb300 import workloads as wl
 
-from gpu_helpers import BF16_RMS_TOL, EMUL_TOL, check_rows, rel_rms, vmax_fp8
+from gpu_helpers import BF16_RMS_TOL, EMUL_TOL, FP8_RMS_TOL, check_rows, rel_rms, vmax_fp8
 
 pytestmark = pytest.mark.gpu
 
-FP8_RMS_TOL = 3e-2
+#: random rows per configuration for the fp64 relative RMS
+N_RANDOM = 512
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -36,17 +41,25 @@ def built():
     fa.load_library()
 
 
-def sample_rows(B, Hq, S, n_random=96, seed=0):
-    """(b, h, i) rows: edges of every 128-row tile near both ends, the first and
-    last rows, and random rows, over a spread of heads."""
-    rng = np.random.default_rng(seed)
+def edge_rows(B, Hq, S):
+    """Edges of the 128-row tiles near both ends, the first and last rows and
+    the middle, for three heads of every batch."""
     edges = sorted({0, 1, 63, 64, 127, 128, 129, 255, 256, S // 2 - 1, S // 2, S - 129,
                     S - 128, S - 127, S - 2, S - 1} & set(range(S)))
     heads = sorted({0, Hq // 2, Hq - 1})
-    rows = [(b, h, i) for b in range(B) for h in heads for i in edges]
-    rows += [(int(rng.integers(0, B)), int(rng.integers(0, Hq)), int(rng.integers(0, S)))
-             for _ in range(n_random)]
-    return np.array(rows, dtype=np.int64)
+    return np.array([(b, h, i) for b in range(B) for h in heads for i in edges], dtype=np.int64)
+
+
+def random_rows(B, Hq, S, n=N_RANDOM, seed=0):
+    """Rows drawn uniformly over (batch, head, row)."""
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.integers(0, B, n), rng.integers(0, Hq, n), rng.integers(0, S, n)],
+                    1).astype(np.int64)
+
+
+def sample_rows(B, Hq, S, n_random=96, seed=0):
+    """Edge rows followed by random rows."""
+    return np.concatenate([edge_rows(B, Hq, S), random_rows(B, Hq, S, n_random, seed)])
 
 
 def pick(out, rows):
@@ -70,56 +83,104 @@ def run_fp8_full(variant, case):
     return res, prod
 
 
-FP8_CONFIGS = [
-    # (name, fp64 gate applies to the scheme at this workload)
-    ("fp8_gqa_h32_8_s16k_d128_outliers", True),
-    ("fp8_h32_s32k_d128", False),
-    ("fp8_mla_h16_s32k_dqk192_dv128_outliers", True),
-]
+#: (GPU variant, oracle path) of the two FP8 paths compared at full size
+FP8_PATHS = {"leanp": (fa.ATTN_VARIANT_LEANP, "leanp"),
+             "ablation": (fa.ATTN_VARIANT_EXACT_FP8, "exact_fp8")}
+FP8_CONFIGS = ["fp8_gqa_h32_8_s16k_d128_outliers", "fp8_h32_s32k_d128",
+               "fp8_mla_h16_s32k_dqk192_dv128_outliers", "fp8_sink_h8_s8k_d128"]
+#: (configuration, path) pairs whose scheme does not meet the 3e-2 fp64 target
+#: on random rows: integer-binade Lean-P on diffuse Gaussian rows at 32K
+#: (about 3.2e-2 in the emulation as well)
+SCHEME_ABOVE_TARGET = {("fp8_h32_s32k_d128", "leanp")}
+
+_results = {}
 
 
-@pytest.mark.parametrize("name,strict", FP8_CONFIGS)
-def test_fp8_fullsize(name, strict):
-    case = wl.make_case(name)
-    B, Hq, Hkv, S, Dqk, Dv = case.shape
-    rows = sample_rows(B, Hq, S)
-    vmax = vmax_fp8(case)
-    ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
+def fullsize(name, path):
+    """GPU output, emulation and ambiguity on edge and random rows, and fp64
+    attention on the random rows, computed once per (configuration, path)."""
+    key = (name, path)
+    if key not in _results:
+        case = wl.make_case(name)
+        B, Hq, Hkv, S, Dqk, Dv = case.shape
+        rows_e, rows_r = edge_rows(B, Hq, S), random_rows(B, Hq, S)
+        rows = np.concatenate([rows_e, rows_r])
+        variant, opath = FP8_PATHS[path]
+        out, prod = run_fp8_full(variant, case)
+        emul, amb, _ = oracle.attention(opath, case.q, case.k, case.v, case.dq, case.dk, case.dv,
+                                        rows=rows)
+        ref = fullsize_ref(name, case, rows_r)
+        _results[key] = dict(case=case, rows=rows, n_edge=len(rows_e), gpu=pick(out, rows),
+                             emul=emul, amb=amb, ref=ref, finite=bool(np.isfinite(out).all()),
+                             prod=None if prod is None else pick(prod, rows))
+    return _results[key]
 
-    # Lean-P
-    out, prod = run_fp8_full(fa.ATTN_VARIANT_LEANP, case)
-    gpu = pick(out, rows)
-    emul, amb = oracle.emul_leanp(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
-    check_rows(gpu, emul, amb, vmax)
-    e_gpu, e_emul = rel_rms(gpu, ref), rel_rms(emul, ref)
-    if strict:
-        assert e_gpu <= FP8_RMS_TOL, (e_gpu, e_emul)
-    else:
-        assert abs(e_gpu - e_emul) <= 0.03 * e_emul and e_gpu <= 3.5e-2, (e_gpu, e_emul)
-    # the bf16 product call is the fp32 result rounded to bf16
-    p = pick(prod, rows)
-    assert np.all(np.abs(p - gpu) <= 2.0 ** -8 * np.abs(gpu) + 1e-6)
-    # nothing outside the sample is left unwritten or non-finite
-    assert np.isfinite(out).all()
-    del out, prod
 
-    # exact-softmax FP8 ablation
-    out, _ = run_fp8_full(fa.ATTN_VARIANT_EXACT_FP8, case)
-    gpu_ab = pick(out, rows)
-    emul_ab, amb_ab = oracle.emul_exact_fp8(case.q, case.k, case.v, case.dq, case.dk, case.dv,
-                                            rows=rows)
-    check_rows(gpu_ab, emul_ab, amb_ab, vmax)
-    e_ab = rel_rms(gpu_ab, ref)
-    assert e_ab <= FP8_RMS_TOL
-    assert np.isfinite(out).all()
-    print(f"{name}: rel-RMS vs fp64 Lean-P {e_gpu:.4f} (emulation {e_emul:.4f}), "
-          f"ablation {e_ab:.4f}, ratio {e_gpu / e_ab:.3f}")
+_refs = {}
+
+
+def fullsize_ref(name, case, rows):
+    if name not in _refs:
+        _refs[name] = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
+    return _refs[name]
+
+
+@pytest.mark.parametrize("path", list(FP8_PATHS))
+@pytest.mark.parametrize("name", FP8_CONFIGS)
+def test_fp8_fullsize_matches_emulation(name, path):
+    r = fullsize(name, path)
+    check_rows(r["gpu"], r["emul"], r["amb"], vmax_fp8(r["case"]))
+    assert r["finite"], "an output outside the sample is not finite"
+    if r["prod"] is not None:  # the bf16 product call is the fp32 result rounded to bf16
+        assert np.all(np.abs(r["prod"] - r["gpu"]) <= 2.0 ** -8 * np.abs(r["gpu"]) + 1e-6)
+    # on the random rows the GPU's fp64 error equals the emulation's within 3%
+    n = r["n_edge"]
+    e_gpu, e_emul = rel_rms(r["gpu"][n:], r["ref"]), rel_rms(r["emul"][n:], r["ref"])
+    print(f"{name} {path}: rel-RMS vs fp64 on {len(r['ref'])} random rows: GPU {e_gpu:.4e}, "
+          f"emulation {e_emul:.4e}")
+    assert abs(e_gpu - e_emul) <= 0.03 * e_emul, (e_gpu, e_emul)
+
+
+def _fp64_gate_params():
+    out = []
+    for name in FP8_CONFIGS:
+        for path in FP8_PATHS:
+            marks = ()
+            if (name, path) in SCHEME_ABOVE_TARGET:
+                marks = pytest.mark.xfail(strict=True, reason=(
+                    "integer-binade Lean-P sits at about 3.2e-2 on diffuse 32K Gaussian rows, "
+                    "in the emulation as well (test_oracle_scheme_floor.py)"))
+            out.append(pytest.param(name, path, marks=marks))
+    return out
+
+
+@pytest.mark.parametrize("name,path", _fp64_gate_params())
+def test_fp8_fullsize_fp64_target(name, path):
+    r = fullsize(name, path)
+    e = rel_rms(r["gpu"][r["n_edge"]:], r["ref"])
+    if ("ablation" in FP8_PATHS) and path == "leanp":
+        ab = fullsize(name, "ablation")
+        e_ab = rel_rms(ab["gpu"][ab["n_edge"]:], ab["ref"])
+        print(f"{name}: Lean-P {e:.4e}, ablation {e_ab:.4e}, ratio {e / e_ab:.3f}")
+    assert e <= FP8_RMS_TOL, e
+
+
+def test_sink_input_block_scale_beats_ablation():
+    """Attention-sink stress input: Lean-P's error against fp64 well below the
+    exact-softmax ablation's (random rows)."""
+    lp, ab = fullsize("fp8_sink_h8_s8k_d128", "leanp"), fullsize("fp8_sink_h8_s8k_d128", "ablation")
+    e_lp = rel_rms(lp["gpu"][lp["n_edge"]:], lp["ref"])
+    e_ab = rel_rms(ab["gpu"][ab["n_edge"]:], ab["ref"])
+    print(f"sink input: rel-RMS vs fp64 Lean-P {e_lp:.3e}, ablation {e_ab:.3e}, "
+          f"ratio {e_lp / e_ab:.3f}")
+    assert e_lp <= 0.5 * e_ab
 
 
 def test_bf16_fullsize():
     case = wl.make_case("bf16_gqa_h32_8_s16k_d128")
     B, Hq, Hkv, S, Dqk, Dv = case.shape
-    rows = sample_rows(B, Hq, S)
+    rows_e, rows_r = edge_rows(B, Hq, S), random_rows(B, Hq, S)
+    rows = np.concatenate([rows_e, rows_r])
     q, k, v = (torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
                for a in (case.q, case.k, case.v))
     out = fa.attn_fwd_ex(fa.ATTN_VARIANT_BF16, q, k, v, out_dtype=fa.ATTN_OUT_F32)
@@ -127,38 +188,16 @@ def test_bf16_fullsize():
     torch.cuda.synchronize()
     out = out.cpu().numpy()
     gpu = pick(out, rows)
-    ref = oracle.ref_fp64_bf16(case.q, case.k, case.v, rows=rows)
-    assert rel_rms(gpu, ref) <= BF16_RMS_TOL
+    ref = oracle.ref_fp64_bf16(case.q, case.k, case.v, rows=rows_r)
+    e = rel_rms(gpu[len(rows_e):], ref)
+    print(f"bf16 16K: rel-RMS vs fp64 on {len(rows_r)} random rows {e:.4e}")
+    assert e <= BF16_RMS_TOL
     emul = oracle.emul_bf16(case.q, case.k, case.v, rows=rows)
     vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
     assert np.max(np.abs(gpu - emul)) <= EMUL_TOL * vmax
     p = pick(prod.float().cpu().numpy(), rows)
     assert np.all(np.abs(p - gpu) <= 2.0 ** -8 * np.abs(gpu) + 1e-6)
     assert np.isfinite(out).all()
-
-
-def test_sink_input():
-    """Attention-sink stress input: parity of both FP8 paths, and Lean-P's
-    error against fp64 well below the exact-softmax ablation's."""
-    case = wl.make_case("fp8_sink_h8_s8k_d128")
-    B, Hq, Hkv, S, Dqk, Dv = case.shape
-    rows = sample_rows(B, Hq, S)
-    vmax = vmax_fp8(case)
-    ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
-    out, _ = run_fp8_full(fa.ATTN_VARIANT_LEANP, case)
-    gpu = pick(out, rows)
-    emul, amb = oracle.emul_leanp(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=rows)
-    check_rows(gpu, emul, amb, vmax)
-    out, _ = run_fp8_full(fa.ATTN_VARIANT_EXACT_FP8, case)
-    gpu_ab = pick(out, rows)
-    emul_ab, amb_ab = oracle.emul_exact_fp8(case.q, case.k, case.v, case.dq, case.dk, case.dv,
-                                            rows=rows)
-    check_rows(gpu_ab, emul_ab, amb_ab, vmax)
-    e_lp, e_ab = rel_rms(gpu, ref), rel_rms(gpu_ab, ref)
-    print(f"sink input: rel-RMS vs fp64 Lean-P {e_lp:.3e}, ablation {e_ab:.3e}, "
-          f"ratio {e_lp / e_ab:.3f}")
-    assert e_lp <= FP8_RMS_TOL
-    assert e_lp <= 0.5 * e_ab
 
 
 def test_noncausal_fullsize_with_per_bkv_descales():

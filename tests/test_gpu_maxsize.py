@@ -62,11 +62,15 @@ def test_output_past_2_31_elements():
         vmax = float(np.max(np.abs(oracle.e4m3_decode(vg)))) * dv
         check_rows(gpu, emul, amb, vmax, EMUL_TOL)
         gpu_all.append(gpu)
+        emul_all.append(emul)
         ref_all.append(ref)
-    err = rel_rms(np.concatenate(gpu_all), np.concatenate(ref_all))
-    print(f"max-size rows: Lean-P rel-RMS vs fp64 {err:.4f}")
-    # diffuse Gaussian rows of 64K-131K keys: the scheme's own error (about 3.2e-2)
-    assert err <= 3.5e-2
+    ref = np.concatenate(ref_all)
+    err, err_emul = rel_rms(np.concatenate(gpu_all), ref), rel_rms(np.concatenate(emul_all), ref)
+    print(f"max-size rows: Lean-P rel-RMS vs fp64 {err:.4f} (emulation {err_emul:.4f})")
+    # Mostly diffuse Gaussian rows of 64K-131K keys, where the scheme's own
+    # error is at the code's floor (tests/test_oracle_scheme_floor.py): the
+    # GPU must carry exactly the emulation's error.
+    assert abs(err - err_emul) <= 0.03 * err_emul, (err, err_emul)
 
 
 def test_long_sequence_chunked_order():
