@@ -460,6 +460,11 @@ def run_ours(args, rank, world, local_rank):
         fa.attn_fwd_ex(fa.ATTN_VARIANT_BLOCK_EXACT, q, k, v, *d, out=out,
                        out_dtype=fa.ATTN_OUT_BF16)
     ms_bx = timed(step_bx, max(3, args.steps // 4), 3)
+    # Lean-P with the code grid anchored at the running row maximum
+    def step_a3():
+        fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP_A3, q, k, v, *d, out=out,
+                       out_dtype=fa.ATTN_OUT_BF16)
+    ms_a3 = timed(step_a3, max(3, args.steps // 4), 3)
     # sustained: back-to-back Lean-P calls for about args.sustained_s seconds,
     # with the SM clock sampled throughout
     n_sus = max(10, int(args.sustained_s * 1e3 / max(ms, 1e-3)))
@@ -517,6 +522,9 @@ def run_ours(args, rank, world, local_rank):
             "block_exact_fp8": {"value": job_tflops(F, world, ms_bx), "ms_per_step": ms_bx,
                                 "note": "Lean-P's block scale and rounded row sum with an "
                                         "exponential in place of the one-FMA code"},
+            "leanp_running_max_anchor": {"value": job_tflops(F, world, ms_a3), "ms_per_step": ms_a3,
+                                         "note": "Lean-P with the code grid anchored at the "
+                                                 "running row maximum (exact O rescale)"},
             "sustained": {"value": job_tflops(F, world, ms_sus), "ms_per_step": ms_sus,
                           "calls": n_sus, "seconds": n_sus * ms_sus / 1e3, "clocks": clk_sus,
                           "tflops_per_ghz": (per_gpu * ms / ms_sus) / (clk_sus["sm_mhz"] / 1e3)
@@ -553,17 +561,31 @@ def run_ours(args, rank, world, local_rank):
             "cores": cores_used(), "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"{len(rows)} random (head, row) pairs of {workload}, oracle_emul_leanp, "
                       f"{dt:.1f} s"}
-        acc_rows = rows[: args.acc_rows]
+        # whole-output relative RMS error against fp64 attention, estimated
+        # from a stratified sample: every row with fewer than 512 keys (about
+        # half of the output's sum of squares) and args.acc_rows weighted rows
+        acc_rows, w = wl.stratified_rows(B, Hq, S, short=512, n_long=args.acc_rows, seed=1)
         ref = oracle.ref_fp64(case.q, case.k, case.v, case.dq, case.dk, case.dv, rows=acc_rows)
-        o_lp = fa.attn_fwd_ex(fa.ATTN_VARIANT_LEANP, q, k, v, *d).cpu().numpy()
-        o_ab = fa.attn_fwd_ex(fa.ATTN_VARIANT_EXACT_FP8, q, k, v, *d).cpu().numpy()
         pick = lambda o, rr: np.stack([o[b, i, h] for b, h, i in rr]).astype(np.float64)
-        rel = lambda x: float(np.sqrt(np.mean((x - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))
-        e_lp, e_ab = rel(pick(o_lp, acc_rows)), rel(pick(o_ab, acc_rows))
-        line["accuracy_sampled_rows"] = {
-            "rows": len(acc_rows), "leanp_rel_rms_vs_fp64": e_lp,
-            "ablation_rel_rms_vs_fp64": e_ab, "leanp_over_ablation": e_lp / e_ab,
-            "leanp_max_abs_vs_emulation": float(np.max(np.abs(pick(o_lp, rows) - emu)))}
+        rel = lambda x: float(np.sqrt(np.sum(w[:, None] * (x - ref) ** 2) /
+                                      np.sum(w[:, None] * ref ** 2)))
+        acc = {}
+        for key, var in (("leanp", fa.ATTN_VARIANT_LEANP), ("ablation", fa.ATTN_VARIANT_EXACT_FP8),
+                         ("leanp_running_max_anchor", fa.ATTN_VARIANT_LEANP_A3)):
+            o = fa.attn_fwd_ex(var, q, k, v, *d).cpu().numpy()
+            acc[key] = rel(pick(o, acc_rows))
+            if key == "leanp":
+                max_abs = float(np.max(np.abs(pick(o, rows) - emu)))
+            del o
+        line["accuracy_whole_output"] = {
+            "estimator": (f"every row i < 512 of every head ({B * Hq * min(512, S)} rows) plus "
+                          f"{args.acc_rows} uniform rows beyond, weighted"),
+            "leanp_rel_rms_vs_fp64": acc["leanp"], "ablation_rel_rms_vs_fp64": acc["ablation"],
+            "leanp_over_ablation": acc["leanp"] / acc["ablation"],
+            "leanp_running_max_anchor_rel_rms_vs_fp64": acc["leanp_running_max_anchor"],
+            "leanp_running_max_anchor_over_ablation":
+                acc["leanp_running_max_anchor"] / acc["ablation"],
+            "leanp_max_abs_vs_emulation": max_abs}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -620,6 +642,7 @@ def extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms, n):
 # --only PATH: the workload each path is profiled on (headline FP8 shape, the
 # BF16 configuration for the BF16 path)
 ONLY_PATHS = {"leanp": "fp8_h32_s32k_d128", "exact_fp8": "fp8_h32_s32k_d128",
+              "leanp_a3": "fp8_h32_s32k_d128",
               "block_exact": "fp8_h32_s32k_d128", "bf16": "bf16_gqa_h32_8_s16k_d128",
               "quantize": "quantize_bf16_s32k_h32_d128",
               "quantize_hadamard": "quantize_bf16_s32k_h32_d128"}
@@ -669,7 +692,8 @@ def run_only(args):
         q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
         d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
         variant = {"leanp": fa.ATTN_VARIANT_LEANP, "exact_fp8": fa.ATTN_VARIANT_EXACT_FP8,
-                   "block_exact": fa.ATTN_VARIANT_BLOCK_EXACT}[args.only]
+                   "block_exact": fa.ATTN_VARIANT_BLOCK_EXACT,
+                   "leanp_a3": fa.ATTN_VARIANT_LEANP_A3}[args.only]
         fn = lambda: fa.attn_fwd_ex(variant, q, k, v, *d, out=out, out_dtype=fa.ATTN_OUT_BF16)
     for _ in range(args.warmup):
         fn()
@@ -786,7 +810,10 @@ def run_sweep(args):
                      # Lean-P's block scale and rounded sum, exponential for the code
                      "block_exact": lambda: fa.attn_fwd_ex(fa.ATTN_VARIANT_BLOCK_EXACT, q, k, v,
                                                            *d, out=out,
-                                                           out_dtype=fa.ATTN_OUT_BF16)}
+                                                           out_dtype=fa.ATTN_OUT_BF16),
+                     "leanp_running_max_anchor": lambda: fa.attn_fwd_ex(
+                         fa.ATTN_VARIANT_LEANP_A3, q, k, v, *d, out=out,
+                         out_dtype=fa.ATTN_OUT_BF16)}
             peak = peaks["bf16_burst"] * FP8_OVER_BF16
             in_bytes = (case.q.nbytes + case.k.nbytes + case.v.nbytes)
         else:
@@ -941,8 +968,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-rows", type=int, default=8192,
                     help="oracle rows timed for cpu_baseline (about 10-30 s of CPU work)")
-    ap.add_argument("--acc-rows", type=int, default=1024,
-                    help="rows compared with fp64 attention for the accuracy report")
+    ap.add_argument("--acc-rows", type=int, default=2048,
+                    help="rows beyond the first 512 of each head compared with fp64 attention "
+                         "for the accuracy report")
     ap.add_argument("--ref-row-budget", type=int, default=8192,
                     help="oracle rows over the whole reference run")
     ap.add_argument("--no-cpu", action="store_true")

@@ -38,6 +38,7 @@ ATTN_VARIANT_LEANP = 0
 ATTN_VARIANT_EXACT_FP8 = 1
 ATTN_VARIANT_BF16 = 2
 ATTN_VARIANT_BLOCK_EXACT = 3  # diagnostic: Lean-P block scale + rounded sum, exact e4m3-rounded p
+ATTN_VARIANT_LEANP_A3 = 4  # Lean-P with the code grid anchored at the running row maximum
 ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 ATTN_FLAG_TEST_STALL_LOADS = 1

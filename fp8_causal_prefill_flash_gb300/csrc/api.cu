@@ -118,7 +118,7 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
         int Dqk, int Dv, int causal, float softmax_scale, int flags, int* dev_status,
         void* stream) {
   // ---- argument checks (before anything touches the device)
-  if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_BLOCK_EXACT) return ATTN_ERR_INVALID_ARG;
+  if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_LEANP_A3) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
@@ -215,6 +215,9 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
     case ATTN_VARIANT_BLOCK_EXACT:
       return Dqk == 128 ? launch<fa8::kBlockExact, 128>(maps, p, sms, s)
                         : launch<fa8::kBlockExact, 192>(maps, p, sms, s);
+    case ATTN_VARIANT_LEANP_A3:
+      return Dqk == 128 ? launch<fa8::kLeanPA3, 128>(maps, p, sms, s)
+                        : launch<fa8::kLeanPA3, 192>(maps, p, sms, s);
     default:
       return launch<fa8::kBf16, 128>(maps, p, sms, s);
   }

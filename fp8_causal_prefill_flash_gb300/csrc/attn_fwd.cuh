@@ -46,6 +46,10 @@
 //              row sum").
 //   kExactFp8  p = 2^(x - m) on the MUFU, rounded to e4m3, unrounded row sum.
 //   kBf16      as kExactFp8 with bf16 operands and probabilities.
+//   kLeanPA3   kLeanP with the code grid anchored at the running row maximum
+//              (the key holding it gets exactly the code of 2^T) instead of at
+//              integer log2 values; O is rescaled exactly whenever the maximum
+//              grows.
 //   kBlockExact  diagnostic: the block exponents, UE8M0 factors and rounded
 //              row sum of kLeanP, but each probability is 2^(x/8 - e + T) from
 //              the MUFU rounded to the nearest e4m3 instead of the Lean-P
@@ -75,7 +79,7 @@ __device__ unsigned long long fa8_timeline[4][64][8];
   } while (0)
 #endif
 
-enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2, kBlockExact = 3 };
+enum Variant : int { kLeanP = 0, kExactFp8 = 1, kBf16 = 2, kBlockExact = 3, kLeanPA3 = 4 };
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per K/V tile
@@ -93,12 +97,16 @@ constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: floats in [2^23, 2^24) hav
 // A row's reference binade is only raised when a block exponent exceeds it
 // by more than this many binades (all rescales are exact powers of two).
 constexpr float kLazyBinades = 8.0f;
+// Running-maximum anchoring (kLeanPA3): the code of a key is
+// floor(8*lam*(s - m) + 8k + C + eps), eps = 2^-6, so the key at the running
+// maximum m gets exactly C, the code of 2^T.
+constexpr float kA3Bias = kLeanC + 1.0f / 64.0f;
 
 template <int V, int DQK>
 struct Cfg {
   static constexpr bool kFp8 = V != kBf16;
   // per-64-key power-of-two block scale and the rounded row sum (O column 128)
-  static constexpr bool kBlockScaled = V == kLeanP || V == kBlockExact;
+  static constexpr bool kBlockScaled = V == kLeanP || V == kBlockExact || V == kLeanPA3;
   static constexpr int kElem = kFp8 ? 1 : 2;
   static constexpr int kRowBytes = DQK * kElem;             // bytes of one Q/K row
   static constexpr int kFullPanels = kRowBytes / 128;       // 128-byte swizzled panels
@@ -109,8 +117,14 @@ struct Cfg {
   static constexpr int kVTileBytes = kBN * kDV * kElem;
   static constexpr int kVPanels = kDV * kElem / 128;
   static constexpr int kStages = kFp8 ? (DQK == 128 ? 4 : 3) : 2;
+  // Q buffers.  With two (FP8 at head dim 128 has the shared memory for them)
+  // the next item's Q tiles load while the current item runs; measured against
+  // one buffer in one session that was 2-5% slower from 2K to 16K keys and on
+  // the sink and GQA workloads, and 1.6% faster at 32K, so one is used.
+  static constexpr int kQBufs = 1;
+  static constexpr int kQBufBytes = 2 * kQkTileBytes;  // both query tiles of an item
   static constexpr int kSmemQ = 0;
-  static constexpr int kSmemK = 2 * kQkTileBytes;
+  static constexpr int kSmemK = kQBufs * kQBufBytes;
   static constexpr int kSmemV = kSmemK + kStages * kQkTileBytes;
   // Lean-P: 128 keys x 128 bytes of e4m3 1.0, the second N-atom of the P.V
   // B operand, so that O's column 128 accumulates the rounded row sum
@@ -197,7 +211,7 @@ __device__ __forceinline__ int kv_tiles_for(const KParams& p, int qb, int t) {
 }
 
 struct __align__(8) Barriers {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];  // per Q buffer
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2];     // S holds S_t(j) (QK commit)
   uint64_t s_drained[2];  // softmax t has copied S into registers
@@ -244,11 +258,13 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
     int b, h, qb;
     decode_item(p, idx, b, h, qb);
     const int g = h / p.group;
-    if (!mbar_wait(&bars.q_empty, (q_it & 1) ^ 1, ab, p.wait_limit_ns)) break;
-    mbar_arrive_expect_tx(&bars.q_full, 2 * C::kQkTileBytes);
-    load_qk_tile<V, DQK>(smem + C::kSmemQ, m, true, &bars.q_full, h, qb * 256, b);
-    load_qk_tile<V, DQK>(smem + C::kSmemQ + C::kQkTileBytes, m, true, &bars.q_full, h,
-                         qb * 256 + 128, b);
+    const uint32_t qbuf = q_it % C::kQBufs, qph = (q_it / C::kQBufs) & 1;
+    if (!mbar_wait(&bars.q_empty[qbuf], qph ^ 1, ab, p.wait_limit_ns)) break;
+    uint8_t* qdst = smem + C::kSmemQ + qbuf * C::kQBufBytes;
+    mbar_arrive_expect_tx(&bars.q_full[qbuf], 2 * C::kQkTileBytes);
+    load_qk_tile<V, DQK>(qdst, m, true, &bars.q_full[qbuf], h, qb * 256, b);
+    load_qk_tile<V, DQK>(qdst + C::kQkTileBytes, m, true, &bars.q_full[qbuf], h, qb * 256 + 128,
+                         b);
     ++q_it;
     const int nkv = kv_tiles_for(p, qb, 1);
     for (int j = 0; j < nkv; ++j, ++kv_it) {
@@ -271,8 +287,9 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
   // Before the CTA may exit, every copy this thread started must have landed:
   // after an abort, and also after a normal end, since a wait in another role
   // may still run out of time while the last loads are in flight.  Only the
-  // last kStages loads of K and of V can be in flight (a stage is reloaded
-  // only after its consumer has waited for the previous load).
+  // last kStages loads of K and of V, and the last kQBufs loads of Q, can be
+  // in flight (a buffer is reloaded only after its consumer has waited for
+  // the previous load).
   // A drain that runs out of time is reported like any other expired wait.
   constexpr uint64_t kDrainNs = 50000000ull;
   volatile int gave_up = 0;
@@ -281,7 +298,8 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
     ok &= mbar_wait(&bars.k_full[i % C::kStages], (i / C::kStages) & 1, &gave_up, kDrainNs);
   for (uint32_t i = nv > (uint32_t)C::kStages ? nv - C::kStages : 0; i < nv; ++i)
     ok &= mbar_wait(&bars.v_full[i % C::kStages], (i / C::kStages) & 1, &gave_up, kDrainNs);
-  if (q_it) ok &= mbar_wait(&bars.q_full, (q_it - 1) & 1, &gave_up, kDrainNs);
+  for (uint32_t i = q_it > (uint32_t)C::kQBufs ? q_it - C::kQBufs : 0; i < q_it; ++i)
+    ok &= mbar_wait(&bars.q_full[i % C::kQBufs], (i / C::kQBufs) & 1, &gave_up, kDrainNs);
   if (!ok) *ab = 1;
 }
 
@@ -289,10 +307,11 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
 // MMA issue.
 // --------------------------------------------------------------------------
 template <int V, int DQK>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, int t, uint32_t k_off) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, uint32_t q_buf_off,
+                                         int t, uint32_t k_off) {
   using C = Cfg<V, DQK>;
   constexpr uint32_t idesc = idesc_f32acc(128, 128, C::kFp8 ? 0 : 1, C::kFp8 ? 0 : 1, 0, 0);
-  const uint32_t q_off = C::kSmemQ + t * C::kQkTileBytes;
+  const uint32_t q_off = q_buf_off + t * C::kQkTileBytes;
 #pragma unroll
   for (int k = 0; k < C::kQkSteps; ++k) {
     const int byte = 32 * k;
@@ -360,7 +379,9 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
     int b, h, qb;
     decode_item(p, idx, b, h, qb);
     const int nk0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
-    if (!mbar_wait(&bars.q_full, q_it & 1, ab, lim)) return;
+    const uint32_t qbuf = q_it % C::kQBufs;
+    const uint32_t q_buf_off = C::kSmemQ + qbuf * C::kQBufBytes;
+    if (!mbar_wait(&bars.q_full[qbuf], (q_it / C::kQBufs) & 1, ab, lim)) return;
     ++q_it;
     for (int j = 0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
@@ -374,7 +395,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
           return;
         if (stamp) FA8_TL(2 + t, j, 4);
         tc_fence_after();
-        issue_qk<V, DQK>(tmem, smem_base, t, C::kSmemK + st * C::kQkTileBytes);
+        issue_qk<V, DQK>(tmem, smem_base, q_buf_off, t, C::kSmemK + st * C::kQkTileBytes);
         // the P.V warp may now queue this tile's previous P.V product behind it
         if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 3]);
         tc_commit(&bars.s_full[t]);
@@ -384,7 +405,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
       }
       tc_commit(&bars.k_empty[st]);
     }
-    tc_commit(&bars.q_empty);
+    tc_commit(&bars.q_empty[qbuf]);
   }
 }
 
@@ -580,7 +601,37 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       float alpha = 1.0f;
       uint32_t pw[C::kPCols];
       uint32_t sfa = 0x7F7F7F7Fu;
-      if constexpr (C::kBlockScaled) {
+      if constexpr (V == kLeanPA3) {
+        // Codes anchored at the running maximum m (raw-score units; lam > 0):
+        // k = floor(lam*(m - block max)) and the bias (8k + C + eps - 8 lam m)/128
+        // per 64-key block.  O and its row-sum column are rescaled by
+        // 2^(lam*(m_old - m_new)) whenever m grows.
+        const float m0 = block_max64(s, 0), m1 = block_max64(s, 64);
+        const float mt = fmaxf(m0, m1);
+        if (!have_ref) {
+          ref = mt;
+          have_ref = true;
+        } else if (mt > ref) {
+          alpha = ex2_approx((ref - mt) * lam);
+          ref = mt;
+          rescale = true;
+        }
+        const bool v0 = m0 > -INFINITY, v1 = m1 > -INFINITY;
+        const float k0 = v0 ? floorf((ref - m0) * lam) : 0.0f;
+        const float k1 = v1 ? floorf((ref - m1) * lam) : 0.0f;
+        // UE8M0 scale 2^(-T-k): byte 127 - T - k, at least 0 (k >= 0)
+        const int x0 = v0 ? (int)fmaxf(127.0f - kLeanT - k0, 0.0f) : 0;
+        const int x1 = v1 ? (int)fmaxf(127.0f - kLeanT - k1, 0.0f) : 0;
+        // a fully masked block has only -inf scores: code 0 whatever the bias
+        const float b0 = v0 ? fmaf(-lam8, ref, 8.0f * k0 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
+        const float b1 = v1 ? fmaf(-lam8, ref, 8.0f * k1 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
+#pragma unroll
+        for (int w = 0; w < 32; ++w)
+          pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
+                               __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
+                               lamc, w < 16 ? b0 : b1, kc);
+        sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
+      } else if constexpr (C::kBlockScaled) {
         const float m0 = block_max64(s, 0), m1 = block_max64(s, 64);
         // block exponents e = ceil(lam*max): the block maximum lands in (2^(T-1), 2^T]
         const float e0 = ceilf(m0 * lam8 * 0.125f), e1 = ceilf(m1 * lam8 * 0.125f);
@@ -664,7 +715,30 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       // P_t(j-1) must have been consumed, and O_t must be final for j-1
       // before it is corrected for a raised reference.
       if (j > 0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
-      if (__any_sync(0xffffffffu, rescale)) {
+      if constexpr (V == kLeanPA3) {
+        // frequent, non-power-of-two: two 64-column passes and the row-sum column
+        if (__any_sync(0xffffffffu, rescale)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 64) {
+            uint32_t o[64];
+            uint32_t (&oa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
+            uint32_t (&ob)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
+            tmem_ld32x2_wait(o_col + c, o_col + c + 32, oa, ob);
+            const uint64_t a2 = f32x2_pack(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const uint64_t y = mul_f32x2(f32x2_pack(__uint_as_float(o[2 * i]),
+                                                      __uint_as_float(o[2 * i + 1])), a2);
+              f32x2_unpack(y, o[2 * i], o[2 * i + 1]);
+            }
+            tmem_st32(o_col + c, oa);
+            tmem_st32(o_col + c + 32, ob);
+          }
+          const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
+          tmem_st1(o_col + 128, __float_as_uint(lv));
+        }
+      } else if (__any_sync(0xffffffffu, rescale)) {
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -699,8 +773,10 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     const float inv = dvv / l;
     // log-sum-exp of the row in natural units: the row sum l is relative to
     // 2^ref (Lean-P: the scaled rounded weights; exact paths: the unrounded p)
+    // the reference in log2 units (the A3 path keeps it in raw-score units)
+    const float ref2 = V == kLeanPA3 ? ref * lam : ref;
     if (p.lse && row < p.S)
-      p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref + log2f(l)) * 0.6931471805599453f;
+      p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
     const bool store = row < p.S;
     const size_t orow = ((size_t)b * p.S + (size_t)(row < p.S ? row : 0)) * p.Hq + h;
 #pragma unroll 1
@@ -750,8 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = warp_id();
   if (threadIdx.x == 0) {
     bars.abort_flag = 0;
-    mbar_init(&bars.q_full, 1);
-    mbar_init(&bars.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.q_full[i], 1);
+      mbar_init(&bars.q_empty[i], 1);
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars.k_full[i], 1);
       mbar_init(&bars.k_empty[i], 1);

@@ -177,3 +177,27 @@ def make_case(name: str, S: Optional[int] = None, **overrides):
                              outliers_qk=cfg.get("outliers_qk", 0),
                              outliers_v=cfg.get("outliers_v", True),
                              factor=cfg.get("factor", 1.0))
+
+
+def stratified_rows(B: int, Hq: int, S: int, short: int = 512, n_long: int = 2048,
+                    seed: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Rows (b, h, i) and weights for estimating a whole-output error sum.
+
+    Causal rows with few keys have large outputs (row 0 is one value row;
+    row i has about |v| / sqrt(i)), so a few hundred short rows hold about
+    half of the output's sum of squares on long sequences, and a uniform
+    sample of rows rarely contains them.  This sample takes every row
+    i < ``short`` of every (b, h) with weight 1, and ``n_long`` rows drawn
+    uniformly from the others with weight (number of other rows) / n_long,
+    so that sum_r w_r f(row r) estimates the sum of f over all B*Hq*S rows.
+    """
+    short = min(short, S)
+    b, h, i = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(short), indexing="ij")
+    rows = [np.stack([b.ravel(), h.ravel(), i.ravel()], 1)]
+    weights = [np.ones(B * Hq * short)]
+    if S > short and n_long > 0:
+        rng = np.random.default_rng(seed)
+        rows.append(np.stack([rng.integers(0, B, n_long), rng.integers(0, Hq, n_long),
+                              rng.integers(short, S, n_long)], 1))
+        weights.append(np.full(n_long, B * Hq * (S - short) / n_long))
+    return np.concatenate(rows).astype(np.int64), np.concatenate(weights)

@@ -96,7 +96,18 @@ typedef enum {
    * what the one-multiply-add code costs in accuracy and saves in time
    * ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X", "Lean P" and
    * "Per-block scaling and a rounded row sum"). */
-  ATTN_VARIANT_BLOCK_EXACT = 3
+  ATTN_VARIANT_BLOCK_EXACT = 3,
+  /* FP8 Lean-P with the code grid anchored at the row's running maximum m:
+   * per 64-key block k = floor(lambda*(m - block max)) and the code
+   * floor(8*lambda*(s - m) + 8k + 112 + 2^-6), clamped to [0, 126], with the
+   * block scale 2^(-7-k); O and the rounded row sum are rescaled exactly by
+   * 2^(lambda*(m_old - m_new)) whenever m grows (per 128-key tile).  The key
+   * holding the maximum gets exactly the code of 2^7.  ATTN_VARIANT_LEANP
+   * anchors the grid at integer log2 values instead (its reference moves only
+   * by powers of two).  Both follow "Lean P: one multiply-add instead of an
+   * exponential" and "Per-block scaling and a rounded row sum", which leave
+   * the anchor of the power-of-two scale open. */
+  ATTN_VARIANT_LEANP_A3 = 4
 } attn_variant;
 
 /* Output element type for attn_fwd_ex. */

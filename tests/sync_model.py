@@ -7,7 +7,8 @@ One persistent CTA runs a list of work items.  Each item has two query tiles
 with ``nk0`` and ``nkv`` key tiles.  The roles are written as generators that
 mirror the kernel's loops operation for operation:
 
-- the producer (Q once per item, K and V through a ring of ``stages``);
+- the producer (Q once per item into one of ``q_bufs`` buffers, K and V
+  through a ring of ``stages``);
 - the QK warp (S products in the order S0(0), S1(0), S0(1), ...);
 - one P.V warp, or one per query tile (``split_pv``);
 - the two softmax groups (copy S out, write P, read O in the epilogue).
@@ -39,7 +40,7 @@ do.
 - From then on a wait that would block returns instead, and its role leaves
   its loop through the kernel's exit sequence.
 - The producer then waits for the loads it may still have in flight (the last
-  ``stages`` of K and of V, and the last Q).
+  ``stages`` of K and of V, and the last ``q_bufs`` of Q).
 - Each issuing warp commits and waits for its own MMAs.
 
 At the CTA's exit, also after a normal run, no TMA load, MMA or commit
@@ -82,12 +83,14 @@ class Protocol:
     """Which variant of the protocol to model (the kernel's is the default:
     4 ``qk_go`` barriers, one P.V warp, a ring of 4 stages)."""
     stages: int = 4
+    q_bufs: int = 1
     order_pv: bool = False
     qk_go: int = 4
     split_pv: bool = False
     # planted mistakes, for the tests that show the checker finds them
     skip_drain_wait: bool = False
     skip_o_done_wait: bool = False
+    skip_q_empty_wait: bool = False
     # the failure path: one bounded wait runs out of time
     inject_timeout: bool = False
     skip_producer_drain: bool = False
@@ -104,7 +107,7 @@ class _State:
     o_free: dict = field(default_factory=dict)   # t -> epilogue has read O_t
     k_stage: dict = field(default_factory=dict)  # st -> (item, j)
     v_stage: dict = field(default_factory=dict)
-    q: int | None = None
+    q: dict = field(default_factory=dict)        # Q buffer -> item
     reads_needed: dict = field(default_factory=dict)  # ('K'|'V'|'Q', version) -> n
     reads_done: dict = field(default_factory=dict)
 
@@ -119,7 +122,8 @@ class Model:
         S = proto.stages
         B = Barrier
         self.bars = {
-            "q_full": B("q_full", 1), "q_empty": B("q_empty", 1),
+            **{f"q_full{i}": B(f"q_full{i}", 1) for i in range(proto.q_bufs)},
+            **{f"q_empty{i}": B(f"q_empty{i}", 1) for i in range(proto.q_bufs)},
             **{f"k_full{i}": B(f"k_full{i}", 1) for i in range(S)},
             **{f"k_empty{i}": B(f"k_empty{i}", 1) for i in range(S)},
             **{f"v_full{i}": B(f"v_full{i}", 1) for i in range(S)},
@@ -164,10 +168,11 @@ class Model:
     def _producer(self):
         S = self.p.stages
         kv_it = 0
+        QB = self.p.q_bufs
         for item, (nk0, nkv) in enumerate(self.items):
-            if item > 0:
-                yield _wait("q_empty", item - 1)
-            yield ("tma", "q_full", "Q", None, item)
+            if item >= QB and not self.p.skip_q_empty_wait:
+                yield _wait(f"q_empty{item % QB}", item // QB - 1)
+            yield ("tma", f"q_full{item % QB}", "Q", item % QB, item)
             for j in range(nkv):
                 st, use = kv_it % S, kv_it // S
                 if use > 0:
@@ -194,8 +199,9 @@ class Model:
             yield ("wait_drain", f"k_full{i % S}", i // S)
         for i in range(max(0, self.n_v - S), self.n_v):
             yield ("wait_drain", f"v_full{i % S}", i // S)
-        if self.n_q:
-            yield ("wait_drain", "q_full", self.n_q - 1)
+        QB = self.p.q_bufs
+        for i in range(max(0, self.n_q - QB), self.n_q):
+            yield ("wait_drain", f"q_full{i % QB}", i // QB)
 
     def _mma_drain(self, name):
         """An issuing warp's last steps, after its loop ends or gives up: its
@@ -219,8 +225,9 @@ class Model:
     def _qk(self):
         S = self.p.stages
         kv_it, issued, last = 0, [0, 0], -1
+        QB = self.p.q_bufs
         for item, (nk0, nkv) in enumerate(self.items):
-            yield _wait("q_full", item)
+            yield _wait(f"q_full{item % QB}", item // QB)
             for j in range(nkv):
                 st, use = kv_it % S, kv_it // S
                 yield _wait(f"k_full{st}", use)
@@ -237,7 +244,7 @@ class Model:
                     last = t
                 yield ("commit", "qk", f"k_empty{st}")
                 kv_it += 1
-            yield ("commit", "qk", "q_empty")
+            yield ("commit", "qk", f"q_empty{item % QB}")
         yield from self._mma_drain("qk")
         yield ("done",)
 
@@ -312,9 +319,11 @@ class Model:
         else:
             self.n_v += 1
         if kind == "Q":
-            if st.q is not None and not self._all_read("Q", st.q):
-                raise Violation(f"Q reloaded for item {version} while products still read item {st.q}")
-            st.q = version
+            old = st.q.get(stage)
+            if old is not None and not self._all_read("Q", old):
+                raise Violation(f"Q buffer {stage} reloaded for item {version} while products "
+                                f"still read item {old}")
+            st.q[stage] = version
             nk0, nkv = self.items[version]
             self._need("Q", version, nk0 + nkv)
         else:
@@ -334,8 +343,10 @@ class Model:
         if kind == "S":
             if not st.s_read:
                 raise Violation(f"S({t},{item},{j}) overwrites S{st.s_content} before it was copied out")
-            if st.k_stage.get(stage) != (item, j) or st.q != item:
-                raise Violation(f"S({t},{item},{j}) reads K stage {stage}={st.k_stage.get(stage)}, Q={st.q}")
+            qbuf = item % self.p.q_bufs
+            if st.k_stage.get(stage) != (item, j) or st.q.get(qbuf) != item:
+                raise Violation(f"S({t},{item},{j}) reads K stage {stage}={st.k_stage.get(stage)}, "
+                                f"Q buffer {qbuf}={st.q.get(qbuf)}")
             self._read("K", (item, j))
             self._read("Q", item)
             st.s_content, st.s_read = (t, item, j), False

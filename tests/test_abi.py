@@ -54,8 +54,10 @@ def call_ex(lib, variant=0, q=P, k=P, v=P, dq=P, dk=P, dv=P, out=P, out_dtype=0,
     (dict(S=0), fa.ATTN_ERR_INVALID_ARG),
     (dict(B=0), fa.ATTN_ERR_INVALID_ARG),
     (dict(variant=7), fa.ATTN_ERR_INVALID_ARG),
-    (dict(variant=4), fa.ATTN_ERR_INVALID_ARG),
+    (dict(variant=5), fa.ATTN_ERR_INVALID_ARG),
     (dict(variant=3, dq=None), fa.ATTN_ERR_INVALID_ARG),       # block-exact is an FP8 path
+    (dict(variant=4, dk=None), fa.ATTN_ERR_INVALID_ARG),       # so is the running-max anchor
+    (dict(variant=4, Dqk=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(variant=3, Dv=64), fa.ATTN_ERR_UNSUPPORTED),
     (dict(out_dtype=3), fa.ATTN_ERR_INVALID_ARG),
     (dict(flags=1), fa.ATTN_ERR_INVALID_ARG),          # stall test hook needs a status word

@@ -39,7 +39,8 @@ def _fp8_parity(variant, case, dq, dk, dv, causal):
                                 return_lse=True)
     torch.cuda.synchronize()
     gpu, glse = out.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
-    path = "leanp" if variant == fa.ATTN_VARIANT_LEANP else "exact_fp8"
+    path = {fa.ATTN_VARIANT_LEANP: "leanp", fa.ATTN_VARIANT_EXACT_FP8: "exact_fp8",
+            fa.ATTN_VARIANT_LEANP_A3: "leanp_a3"}[variant]
     emul, amb, else_ = oracle.attention(path, case.q, case.k, case.v, dq, dk, dv, causal=causal)
     check_rows(gpu, emul, amb, _vmax(case, dv))
     # log-sum-exp: the row sums agree up to the weight mass near a rounding
@@ -51,14 +52,16 @@ def _fp8_parity(variant, case, dq, dk, dv, causal):
 
 
 @pytest.mark.parametrize("S", [1, 100, 257, 600])
-@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 def test_noncausal_fp8(S, variant):
     case = wl.fp8_gaussian_case(1, 4, 2, S, 128, 128, seeds=(101, 102, 103))
     _fp8_parity(variant, case, case.dq, case.dk, case.dv, causal=False)
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 def test_per_bkv_descales(causal, variant):
     B, Hq, Hkv = 2, 4, 2
     case = wl.fp8_gaussian_case(B, Hq, Hkv, 333, 128, 128, seeds=(104, 105, 106))
@@ -118,7 +121,8 @@ def test_flash_attn_style_wrappers():
 
 @pytest.mark.parametrize("S", [1, 129, 511])
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 def test_mla_gqa_batched_options(S, causal, variant):
     """The MLA shape (Dqk 192, Dv 128) with GQA, B = 2, descales per (batch,
     kv head) and the LSE, over ragged lengths, causal and not."""

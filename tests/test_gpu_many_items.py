@@ -22,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 B, HQ, HKV = 8, 32, 8
 PATHS = {fa.ATTN_VARIANT_LEANP: "leanp", fa.ATTN_VARIANT_EXACT_FP8: "exact_fp8",
-         fa.ATTN_VARIANT_BLOCK_EXACT: "variant_e", fa.ATTN_VARIANT_BF16: "bf16"}
+         fa.ATTN_VARIANT_BLOCK_EXACT: "variant_e", fa.ATTN_VARIANT_BF16: "bf16",
+         fa.ATTN_VARIANT_LEANP_A3: "leanp_a3"}
 
 
 @pytest.fixture(scope="module", autouse=True)

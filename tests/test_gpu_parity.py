@@ -189,7 +189,7 @@ def test_bitwise_identical_over_7200_launches():
 
 
 @pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_BLOCK_EXACT,
-                                     fa.ATTN_VARIANT_BF16])
+                                     fa.ATTN_VARIANT_BF16, fa.ATTN_VARIANT_LEANP_A3])
 @pytest.mark.parametrize("causal", [True, False])
 def test_every_variant_is_deterministic(variant, causal):
     """Every path, causal or not, with fp32 output and the log-sum-exp: 20
@@ -256,7 +256,8 @@ def test_argument_errors_are_reported():
 # ------------------------------------------------------------------ out-of-bounds writes
 
 @pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
-                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16])
+                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 @pytest.mark.parametrize("S,causal", [(1, True), (65, True), (300, False), (257, True)])
 @pytest.mark.parametrize("out_dtype", [fa.ATTN_OUT_BF16, fa.ATTN_OUT_F32])
 def test_no_write_outside_output_and_lse(variant, S, causal, out_dtype):
@@ -306,7 +307,8 @@ def test_no_write_outside_output_and_lse(variant, S, causal, out_dtype):
 # ------------------------------------------------------------------ item order
 
 @pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
-                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16])
+                                     fa.ATTN_VARIANT_BLOCK_EXACT, fa.ATTN_VARIANT_BF16,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 @pytest.mark.parametrize("causal", [True, False])
 def test_chunked_item_order_gives_the_same_bits(variant, causal):
     """Work items chunked by (batch, kv head), the order used for problems
@@ -329,7 +331,8 @@ def test_chunked_item_order_gives_the_same_bits(variant, causal):
 # ------------------------------------------------------------------ extreme ranges
 
 @pytest.mark.parametrize("spread", [50.0, 300.0])
-@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8])
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_EXACT_FP8,
+                                     fa.ATTN_VARIANT_LEANP_A3])
 def test_extreme_logit_ranges(spread, variant):
     """Descales that spread the logits over hundreds of nats: the lazy
     reference must move by exact powers of two, far-below blocks clamp their
@@ -348,7 +351,8 @@ def test_extreme_logit_ranges(spread, variant):
     torch.cuda.synchronize()
     gpu = out.cpu().numpy().astype(np.float64)
     assert np.isfinite(gpu).all()
-    path = "leanp" if variant == fa.ATTN_VARIANT_LEANP else "exact_fp8"
+    path = {fa.ATTN_VARIANT_LEANP: "leanp", fa.ATTN_VARIANT_EXACT_FP8: "exact_fp8",
+            fa.ATTN_VARIANT_LEANP_A3: "leanp_a3"}[variant]
     emul, amb, _ = oracle.attention(path, case.q, case.k, case.v, dq, dk, case.dv)
     check_rows(gpu.reshape(-1, 128), emul.reshape(-1, 128), amb.reshape(-1), vmax_fp8(case))
 

@@ -7,7 +7,8 @@ schedules with random per-role speeds.
   stages and four ``qk_go`` barriers per tile.
 - Mistakes planted in the model are found: two ``qk_go`` barriers per tile
   alias (a first GPU build of that variant ended some launches on the bounded
-  wait's timeout), and dropping the S-drain or P.V-done wait is an overwrite.
+  wait's timeout), and dropping the S-drain, P.V-done or Q-empty wait is an
+  overwrite.
 - The failure path: with one bounded wait running out of time at a random
   moment, every role leaves and the CTA exits with no TMA load, MMA or commit
   arrival in flight; without the producer's or an issuing warp's drain it
@@ -25,12 +26,13 @@ SEEDS = range(400)
 
 
 @pytest.mark.parametrize("proto", [
-    sm.Protocol(stages=4),                               # FP8, Dqk 128
-    sm.Protocol(stages=3),                               # FP8, Dqk 192
-    sm.Protocol(stages=2, order_pv=True, qk_go=4),       # BF16
+    sm.Protocol(stages=4, q_bufs=1),                     # FP8, Dqk 128
+    sm.Protocol(stages=3, q_bufs=1),                     # FP8, Dqk 192
+    sm.Protocol(stages=2, q_bufs=1, order_pv=True, qk_go=4),  # BF16
+    sm.Protocol(stages=4, q_bufs=2),                     # FP8 with two Q buffers
     sm.Protocol(stages=4, order_pv=True, qk_go=4),       # the order with a deeper ring
     sm.Protocol(stages=4, order_pv=True, qk_go=4, split_pv=True),
-], ids=["fp8", "fp8_mla", "bf16", "ordered_4stages", "ordered_split"])
+], ids=["fp8", "fp8_mla", "bf16", "fp8_two_q", "ordered_4stages", "ordered_split"])
 def test_kernel_protocols_have_no_race_or_aliasing(proto):
     assert sm.check(proto, SEEDS) is None
 
@@ -52,6 +54,13 @@ def test_missing_drain_wait_is_an_overwrite_of_s():
     assert found is not None and "before it was copied out" in found[2], found
 
 
+def test_missing_q_empty_wait_is_an_overwrite_of_q():
+    # the producer reloading a Q buffer before the S products of its previous
+    # item have run
+    found = sm.check(sm.Protocol(q_bufs=2, skip_q_empty_wait=True), SEEDS)
+    assert found is not None and "Q buffer" in found[2], found
+
+
 def test_missing_pv_done_wait_is_an_overwrite_of_p():
     found = sm.check(sm.Protocol(skip_o_done_wait=True), SEEDS)
     assert found is not None and "before its P.V ran" in found[2], found
@@ -63,17 +72,18 @@ def test_model_reports_a_deadlock():
     import random
     items = [(1, 2), (2, 2)]
     m = sm.Model(items, sm.Protocol(), random.Random(0))
-    m.bars["q_full"].count = 2
-    m.bars["q_full"].pending = 2
+    m.bars["q_full0"].count = 2
+    m.bars["q_full0"].pending = 2
     with pytest.raises(sm.Violation, match="deadlock"):
         m.run()
 
 
 @pytest.mark.parametrize("proto", [
-    sm.Protocol(stages=4, inject_timeout=True),
-    sm.Protocol(stages=3, inject_timeout=True),
-    sm.Protocol(stages=2, order_pv=True, inject_timeout=True),
-], ids=["fp8", "fp8_mla", "bf16"])
+    sm.Protocol(stages=4, q_bufs=1, inject_timeout=True),
+    sm.Protocol(stages=4, q_bufs=2, inject_timeout=True),
+    sm.Protocol(stages=3, q_bufs=1, inject_timeout=True),
+    sm.Protocol(stages=2, q_bufs=1, order_pv=True, inject_timeout=True),
+], ids=["fp8", "fp8_two_q", "fp8_mla", "bf16"])
 def test_a_timed_out_wait_leaves_nothing_in_flight(proto):
     assert sm.check(proto, range(600)) is None
 
