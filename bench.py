@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3934927104,
-                    "sources_sha256": "8a556ebfa7a67c6be902ec8c56aba79a8e173eea63dd87ef1b5b00e6b5444e3f"}
+PROFILED_TRAFFIC = {"bytes": 3929015296,
+                    "sources_sha256": "751bd9b12913ad4af5404deaabba4db48dbdb718484e8d3347de6ebe0334dcf0"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

@@ -57,6 +57,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -141,6 +142,12 @@ struct Cfg {
   // slower: there the P.V warp's issue-and-drain then delays P.V past the
   // point where the softmax needs it.
   static constexpr bool kOrderPv = !kFp8;
+  // P written and announced in two 64-key halves, each P.V product issued as
+  // two pairs of K-steps, the first as soon as its half is in tensor memory.
+  // Measured against whole P in one session: 1.2% (integer binades) and 2.1%
+  // (running-maximum anchor) faster at the MLA shape, where the S product is
+  // six MMAs, but 1-3% slower at head dim 128 and slower on the exact paths.
+  static constexpr bool kPHalves = DQK == 192 && (V == kLeanP || V == kLeanPA3);
   // tensor-memory columns
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColP0 = 128, kColP1 = kFp8 ? 176 : 192;
@@ -216,6 +223,7 @@ struct __align__(8) Barriers {
   uint64_t s_full[2];     // S holds S_t(j) (QK commit)
   uint64_t s_drained[2];  // softmax t has copied S into registers
   uint64_t p_full[2];     // softmax t has written P_t(j)
+  uint64_t p_half[2];     // softmax t has written the first 64 keys of P_t(j) (FP8)
   uint64_t o_done[2];     // PV_t(j) complete (PV commit)
   uint64_t qk_go[2][4];   // S product n of tile t issued: qk_go[t][n % 4] (BF16)
   uint64_t o_free[2];     // softmax t has read O_t in its epilogue
@@ -333,7 +341,8 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t smem_base, uint
   }
 }
 
-template <int V, int DQK>
+// K-steps K0 .. K1-1 of O_t (+)= P_t V (32 keys per FP8 step, 16 per BF16 step).
+template <int V, int DQK, int K0, int K1>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int t, uint32_t v_off,
                                          bool accumulate) {
   using C = Cfg<V, DQK>;
@@ -345,7 +354,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int 
     // at LBO after the V stage; N = 128 otherwise.
     const uint32_t lbo = C::kOnesBytes ? (uint32_t)(C::kSmemOnes - (int)v_off) : 1024u;
 #pragma unroll
-    for (int k = 0; k < C::kPvSteps; ++k) {
+    for (int k = K0; k < K1; ++k) {
       const uint64_t bdesc = smem_desc(smem_base + v_off + 4096 * k, lbo, 1024, kSwizzle128B);
       mma_mx8_ts(d, a + 8 * k, bdesc, idesc_mx(128, C::kPvN, 0, 0, 0, 1, k, k), a + 32,
                  tmem + C::kColSfb, accumulate || k > 0);
@@ -353,7 +362,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int 
   } else {
     constexpr uint32_t idesc = idesc_f32acc(128, 128, 1, 1, 0, 1);
 #pragma unroll
-    for (int k = 0; k < C::kPvSteps; ++k) {
+    for (int k = K0; k < K1; ++k) {
       const uint64_t bdesc =
           smem_desc(smem_base + v_off + 2048 * k, C::kPanelBytes, 1024, kSwizzle128B);
       mma_f16_ts(d, a + 8 * k, bdesc, idesc, accumulate || k > 0);
@@ -444,8 +453,8 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
       for (int t = 0; t < 2; ++t) {
         if (j >= (t ? nkv : nk0)) continue;
         if (stamp) FA8_TL(2 + t, j, 0);
-        if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
-        ++p_cnt[t];
+        if (!mbar_wait(C::kPHalves ? &bars.p_half[t] : &bars.p_full[t], p_cnt[t] & 1, ab, lim))
+          return;
         if (j == 0) {
           // the previous item's epilogue must have read O_t
           if (!mbar_wait(&bars.o_free[t], (items & 1) ^ 1, ab, lim)) return;
@@ -459,7 +468,16 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         }
         if (stamp) FA8_TL(2 + t, j, 1);
         tc_fence_after();
-        issue_pv<V, DQK>(tmem, smem_base, t, C::kSmemV + st * C::kVTileBytes, j > 0);
+        const uint32_t v_off = C::kSmemV + st * C::kVTileBytes;
+        if constexpr (C::kPHalves) {
+          issue_pv<V, DQK, 0, 2>(tmem, smem_base, t, v_off, j > 0);
+          if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
+          tc_fence_after();
+          issue_pv<V, DQK, 2, 4>(tmem, smem_base, t, v_off, true);
+        } else {
+          issue_pv<V, DQK, 0, C::kPvSteps>(tmem, smem_base, t, v_off, j > 0);
+        }
+        ++p_cnt[t];
         tc_commit(&bars.o_done[t]);
         if (stamp) FA8_TL(2 + t, j, 2);
       }
@@ -601,6 +619,11 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       float alpha = 1.0f;
       uint32_t pw[C::kPCols];
       uint32_t sfa = 0x7F7F7F7Fu;
+      // per-tile constants of the code step: the bias of each 64-key block
+      // (Lean-P paths), the exponent offset of each block (block-exact), or
+      // minus the running maximum (exact paths)
+      float cb0 = 0.0f, cb1 = 0.0f;
+      float ls0 = 0.f, ls1 = 0.f;  // exact paths: row sum of the unrounded p
       if constexpr (V == kLeanPA3) {
         // Codes anchored at the running maximum m (raw-score units; lam > 0):
         // k = floor(lam*(m - block max)) and the bias (8k + C + eps - 8 lam m)/128
@@ -623,13 +646,8 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         const int x0 = v0 ? (int)fmaxf(127.0f - kLeanT - k0, 0.0f) : 0;
         const int x1 = v1 ? (int)fmaxf(127.0f - kLeanT - k1, 0.0f) : 0;
         // a fully masked block has only -inf scores: code 0 whatever the bias
-        const float b0 = v0 ? fmaf(-lam8, ref, 8.0f * k0 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
-        const float b1 = v1 ? fmaf(-lam8, ref, 8.0f * k1 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
-#pragma unroll
-        for (int w = 0; w < 32; ++w)
-          pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
-                               __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
-                               lamc, w < 16 ? b0 : b1, kc);
+        cb0 = v0 ? fmaf(-lam8, ref, 8.0f * k0 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
+        cb1 = v1 ? fmaf(-lam8, ref, 8.0f * k1 + kA3Bias) * (1.0f / 128.0f) : 0.0f;
         sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
       } else if constexpr (C::kBlockScaled) {
         const float m0 = block_max64(s, 0), m1 = block_max64(s, 64);
@@ -649,27 +667,15 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
         const bool v0 = e0 > -INFINITY, v1 = e1 > -INFINITY;
         const int x0 = v0 ? max(min((int)(e0 - ref) - kLeanT + 127, 254), 0) : 0;
         const int x1 = v1 ? max(min((int)(e1 - ref) - kLeanT + 127, 254), 0) : 0;
-        // bias per block: (C - 8e)/128, exact; a fully masked block has only
-        // -inf scores, which give code 0 whatever the bias
-        const float b0 = v0 ? (kLeanC - 8.0f * e0) * (1.0f / 128.0f) : 0.0f;
-        const float b1 = v1 ? (kLeanC - 8.0f * e1) * (1.0f / 128.0f) : 0.0f;
         if constexpr (V == kLeanP) {
-#pragma unroll
-          for (int w = 0; w < 32; ++w)
-            pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
-                                 __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
-                                 lamc, w < 16 ? b0 : b1, kc);
+          // bias per block: (C - 8e)/128, exact; a fully masked block has only
+          // -inf scores, which give code 0 whatever the bias
+          cb0 = v0 ? (kLeanC - 8.0f * e0) * (1.0f / 128.0f) : 0.0f;
+          cb1 = v1 ? (kLeanC - 8.0f * e1) * (1.0f / 128.0f) : 0.0f;
         } else {
           // exponent x/8 - e + T = s*lam + (T - e); masked keys (-inf) give 0
-          const float g0 = v0 ? (float)kLeanT - e0 : 0.0f, g1 = v1 ? (float)kLeanT - e1 : 0.0f;
-#pragma unroll
-          for (int w = 0; w < 32; ++w) {
-            const float g = w < 16 ? g0 : g1;
-            float pv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, g));
-            pw[w] = f32x2_to_e4m3x2(pv[0], pv[1]) | (f32x2_to_e4m3x2(pv[2], pv[3]) << 16);
-          }
+          cb0 = v0 ? (float)kLeanT - e0 : 0.0f;
+          cb1 = v1 ? (float)kLeanT - e1 : 0.0f;
         }
         // scale factor bytes: K-steps 0-1 (block 0) and 2-3 (block 1)
         sfa = (uint32_t)x0 | ((uint32_t)x0 << 8) | ((uint32_t)x1 << 16) | ((uint32_t)x1 << 24);
@@ -683,15 +689,34 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           ref = mt;
           rescale = true;
         }
-        const float nb = -ref;
-        float ls0 = 0.f, ls1 = 0.f;
-        if constexpr (V == kExactFp8) {
+        cb0 = cb1 = -ref;
+      }
+      // The code step for words [W0, W1) of P (4 FP8 or 2 BF16 probabilities
+      // per 32-bit word; words 0-15 hold the first 64-key block on FP8).
+      auto codes = [&](auto w0c, auto w1c) {
+        constexpr int W0 = decltype(w0c)::value, W1 = decltype(w1c)::value;
+        if constexpr (V == kLeanP || V == kLeanPA3) {
 #pragma unroll
-          for (int w = 0; w < 32; ++w) {
+          for (int w = W0; w < W1; ++w)
+            pw[w] = leanp_codes4(__uint_as_float(s[4 * w]), __uint_as_float(s[4 * w + 1]),
+                                 __uint_as_float(s[4 * w + 2]), __uint_as_float(s[4 * w + 3]),
+                                 lamc, w < 16 ? cb0 : cb1, kc);
+        } else if constexpr (V == kBlockExact) {
+#pragma unroll
+          for (int w = W0; w < W1; ++w) {
+            const float g = w < 16 ? cb0 : cb1;
+            float pv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, g));
+            pw[w] = f32x2_to_e4m3x2(pv[0], pv[1]) | (f32x2_to_e4m3x2(pv[2], pv[3]) << 16);
+          }
+        } else if constexpr (V == kExactFp8) {
+#pragma unroll
+          for (int w = W0; w < W1; ++w) {
             float pv[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, nb));
+              pv[i] = ex2_approx(fmaf(__uint_as_float(s[4 * w + i]), lam, cb0));
             ls0 += pv[0] + pv[2];
             ls1 += pv[1] + pv[3];
             const uint32_t lo = f32x2_to_e4m3x2(pv[0], pv[1]);
@@ -700,65 +725,87 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           }
         } else {
 #pragma unroll
-          for (int w = 0; w < 64; ++w) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * w]), lam, nb));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * w + 1]), lam, nb));
+          for (int w = W0; w < W1; ++w) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * w]), lam, cb0));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * w + 1]), lam, cb0));
             ls0 += p0;
             ls1 += p1;
             __nv_bfloat162 hv = __floats2bfloat162_rn(p0, p1);
             pw[w] = *reinterpret_cast<uint32_t*>(&hv);
           }
         }
-        l = l * alpha + (ls0 + ls1);
-      }
-      if (stamp) FA8_TL(t, j, 3);
+      };
       // P_t(j-1) must have been consumed, and O_t must be final for j-1
       // before it is corrected for a raised reference.
-      if (j > 0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
-      if constexpr (V == kLeanPA3) {
-        // frequent, non-power-of-two: two 64-column passes and the row-sum column
-        if (__any_sync(0xffffffffu, rescale)) {
+      auto wait_o_and_rescale = [&]() -> bool {
+        if (j > 0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return false;
+        if constexpr (V == kLeanPA3) {
+          // frequent, non-power-of-two: 32-column passes with packed multiplies
+          // (the second block's scores are still live here) and the row-sum column
+          if (__any_sync(0xffffffffu, rescale)) {
+            tc_fence_after();
+            const uint64_t a2 = f32x2_pack(alpha, alpha);
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+              uint32_t o[32];
+              tmem_ld32_wait(o_col + c, o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const uint64_t y = mul_f32x2(f32x2_pack(__uint_as_float(o[2 * i]),
+                                                        __uint_as_float(o[2 * i + 1])), a2);
+                f32x2_unpack(y, o[2 * i], o[2 * i + 1]);
+              }
+              tmem_st32(o_col + c, o);
+            }
+            const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
+            tmem_st1(o_col + 128, __float_as_uint(lv));
+          }
+        } else if (__any_sync(0xffffffffu, rescale)) {
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 64) {
-            uint32_t o[64];
-            uint32_t (&oa)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
-            uint32_t (&ob)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
-            tmem_ld32x2_wait(o_col + c, o_col + c + 32, oa, ob);
-            const uint64_t a2 = f32x2_pack(alpha, alpha);
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t o[32];
+            tmem_ld32_wait(o_col + c, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const uint64_t y = mul_f32x2(f32x2_pack(__uint_as_float(o[2 * i]),
-                                                      __uint_as_float(o[2 * i + 1])), a2);
-              f32x2_unpack(y, o[2 * i], o[2 * i + 1]);
-            }
-            tmem_st32(o_col + c, oa);
-            tmem_st32(o_col + c + 32, ob);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(o_col + c, o);
           }
-          const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
-          tmem_st1(o_col + 128, __float_as_uint(lv));
+          if constexpr (C::kBlockScaled) {  // the row-sum column
+            const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
+            tmem_st1(o_col + 128, __float_as_uint(lv));
+          }
         }
-      } else if (__any_sync(0xffffffffu, rescale)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-          uint32_t o[32];
-          tmem_ld32_wait(o_col + c, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(o_col + c, o);
-        }
-        if constexpr (C::kBlockScaled) {  // the row-sum column
-          const float lv = __uint_as_float(tmem_ld1_wait(o_col + 128)) * alpha;
-          tmem_st1(o_col + 128, __float_as_uint(lv));
-        }
-      }
-      if constexpr (C::kFp8) {
-        tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+        return true;
+      };
+      using W0 = std::integral_constant<int, 0>;
+      using W16 = std::integral_constant<int, 16>;
+      using W32 = std::integral_constant<int, 32>;
+      if constexpr (C::kPHalves) {
+        // first 64-key block: its codes and both blocks' scale factors, then
+        // the P.V warp may issue K-steps 0-1 while the second block is coded
+        codes(W0{}, W16{});
+        if (stamp) FA8_TL(t, j, 3);
+        if (!wait_o_and_rescale()) return;
+        tmem_st16(p_col, *reinterpret_cast<uint32_t(*)[16]>(&pw[0]));
         tmem_st1(p_col + 32 + quad, sfa);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.p_half[t]);
+        codes(W16{}, W32{});
+        tmem_st16(p_col + 16, *reinterpret_cast<uint32_t(*)[16]>(&pw[16]));
+        if constexpr (!C::kBlockScaled) l = l * alpha + (ls0 + ls1);
       } else {
-        tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
-        tmem_st32(p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
+        codes(W0{}, std::integral_constant<int, C::kPCols>{});
+        if constexpr (!C::kBlockScaled) l = l * alpha + (ls0 + ls1);
+        if (stamp) FA8_TL(t, j, 3);
+        if (!wait_o_and_rescale()) return;
+        if constexpr (C::kFp8) {
+          tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+          tmem_st1(p_col + 32 + quad, sfa);
+        } else {
+          tmem_st32(p_col, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+          tmem_st32(p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
+        }
       }
       tmem_st_wait();
       tc_fence_before();
@@ -840,6 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_full[t], 1);
       mbar_init(&bars.s_drained[t], 128);
       mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.p_half[t], 128);
       mbar_init(&bars.o_done[t], 1);
       for (int i = 0; i < 4; ++i) mbar_init(&bars.qk_go[t][i], 1);
       mbar_init(&bars.o_free[t], 128);

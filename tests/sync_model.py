@@ -13,6 +13,10 @@ mirror the kernel's loops operation for operation:
 - one P.V warp, or one per query tile (``split_pv``);
 - the two softmax groups (copy S out, write P, read O in the epilogue).
 
+With ``p_halves`` P is written and announced in two 64-key halves
+(``p_half`` after the first, ``p_full`` after the second) and each P.V
+product is issued as two MMAs, one per half, each after its half.
+
 With ``order_pv`` the P.V product of key tile j waits until the tile's S
 product of key tile j+1 has been issued, through ``qk_go`` barriers (the BF16
 schedule).  ``qk_go`` sets how many barriers each tile has.
@@ -84,6 +88,7 @@ class Protocol:
     4 ``qk_go`` barriers, one P.V warp, a ring of 4 stages)."""
     stages: int = 4
     q_bufs: int = 1
+    p_halves: bool = False
     order_pv: bool = False
     qk_go: int = 4
     split_pv: bool = False
@@ -101,7 +106,7 @@ class Protocol:
 class _State:
     s_content: tuple | None = None  # (t, item, j) of the S product in S
     s_read: bool = True
-    p: dict = field(default_factory=dict)        # t -> [(item, j), consumed]
+    p: dict = field(default_factory=dict)        # t -> [(item, j), consumed, halves written]
     o_item: dict = field(default_factory=dict)   # t -> item accumulating in O_t
     o_done_n: dict = field(default_factory=dict) # t -> P.V products run for o_item
     o_free: dict = field(default_factory=dict)   # t -> epilogue has read O_t
@@ -131,6 +136,7 @@ class Model:
             **{f"s_full{t}": B(f"s_full{t}", 1) for t in range(2)},
             **{f"s_drained{t}": B(f"s_drained{t}", 1) for t in range(2)},
             **{f"p_full{t}": B(f"p_full{t}", 1) for t in range(2)},
+            **{f"p_half{t}": B(f"p_half{t}", 1) for t in range(2)},
             **{f"o_done{t}": B(f"o_done{t}", 1) for t in range(2)},
             **{f"o_free{t}": B(f"o_free{t}", 1) for t in range(2)},
             **{f"qk_go{t}_{i}": B(f"qk_go{t}_{i}", 1) for t in range(2) for i in range(proto.qk_go)},
@@ -140,7 +146,7 @@ class Model:
         self.n_k = self.n_v = self.n_q = 0  # loads the producer has issued
         self.st = _State()
         for t in range(2):
-            self.st.p[t] = [None, True]
+            self.st.p[t] = [None, True, 2]
             self.st.o_item[t] = None
             self.st.o_done_n[t] = 0
             self.st.o_free[t] = True
@@ -260,8 +266,10 @@ class Model:
                     nk = nkv if t else nk0
                     if j >= nk:
                         continue
-                    yield _wait(f"p_full{t}", p_cnt[t])
-                    p_cnt[t] += 1
+                    if self.p.p_halves:
+                        yield _wait(f"p_half{t}", p_cnt[t])
+                    else:
+                        yield _wait(f"p_full{t}", p_cnt[t])
                     if j == 0 and item > 0:
                         yield _wait(f"o_free{t}", item - 1)
                     if self.p.order_pv:
@@ -269,7 +277,13 @@ class Model:
                         while go_seen[t] <= upto:
                             yield _wait(f"qk_go{t}_{go_seen[t] % G}", go_seen[t] // G)
                             go_seen[t] += 1
-                    yield ("mma", name, "PV", (t, item, j, st))
+                    if self.p.p_halves:
+                        yield ("mma", name, "PVa", (t, item, j, st))
+                        yield _wait(f"p_full{t}", p_cnt[t])
+                        yield ("mma", name, "PVb", (t, item, j, st))
+                    else:
+                        yield ("mma", name, "PV", (t, item, j, st))
+                    p_cnt[t] += 1
                     yield ("commit", name, f"o_done{t}")
                 yield ("commit", name, f"v_empty{w}_{st}")
                 kv_it += 1
@@ -289,7 +303,12 @@ class Model:
                 yield ("arrive", f"s_drained{t}")
                 if j > 0 and not self.p.skip_o_done_wait:
                     yield _wait(f"o_done{t}", o_cnt - 1)
-                yield ("write_p", t, item, j)
+                if self.p.p_halves:
+                    yield ("write_p_half", t, item, j, 0)
+                    yield ("arrive", f"p_half{t}")
+                    yield ("write_p_half", t, item, j, 1)
+                else:
+                    yield ("write_p", t, item, j)
                 yield ("arrive", f"p_full{t}")
                 o_cnt += 1
             yield _wait(f"o_done{t}", o_cnt - 1)
@@ -351,20 +370,25 @@ class Model:
             self._read("Q", item)
             st.s_content, st.s_read = (t, item, j), False
         else:
-            pc, consumed = st.p[t]
-            if pc != (item, j) or consumed:
-                raise Violation(f"PV({t},{item},{j}) reads P_{t}={pc} (consumed {consumed})")
+            # PV: the whole product; PVa / PVb: its halves (keys 0-63 / 64-127)
+            pc, consumed, halves = st.p[t]
+            need = 1 if kind == "PVa" else 2
+            if pc != (item, j) or consumed or halves < need:
+                raise Violation(f"{kind}({t},{item},{j}) reads P_{t}={pc} (consumed {consumed}, "
+                                f"{halves} halves written)")
             if st.v_stage.get(stage) != (item, j):
-                raise Violation(f"PV({t},{item},{j}) reads V stage {stage}={st.v_stage.get(stage)}")
-            if j == 0:
+                raise Violation(f"{kind}({t},{item},{j}) reads V stage {stage}={st.v_stage.get(stage)}")
+            first = kind in ("PV", "PVa")
+            if j == 0 and first:
                 if not st.o_free[t]:
                     raise Violation(f"PV({t},{item},0) overwrites O_{t} before the epilogue read it")
                 st.o_item[t], st.o_done_n[t], st.o_free[t] = item, 0, False
             elif st.o_item[t] != item:
-                raise Violation(f"PV({t},{item},{j}) accumulates into O_{t} of item {st.o_item[t]}")
-            st.o_done_n[t] += 1
-            st.p[t][1] = True
-            self._read("V", (item, j))
+                raise Violation(f"{kind}({t},{item},{j}) accumulates into O_{t} of item {st.o_item[t]}")
+            if kind in ("PV", "PVb"):
+                st.o_done_n[t] += 1
+                st.p[t][1] = True
+                self._read("V", (item, j))
 
     def _role_op(self, name, op):
         st = self.st
@@ -384,12 +408,17 @@ class Model:
             if st.s_content != (t, item, j) or st.s_read:
                 raise Violation(f"softmax {t} copies out S{st.s_content} expecting ({t},{item},{j})")
             st.s_read = True
-        elif kind == "write_p":
-            _, t, item, j = op
-            pc, consumed = st.p[t]
+        elif kind == "write_p" or (kind == "write_p_half" and op[4] == 0):
+            t, item, j = op[1:4]
+            pc, consumed, _ = st.p[t]
             if pc is not None and not consumed:
                 raise Violation(f"softmax {t} writes P({item},{j}) over P{pc} before its P.V ran")
-            st.p[t] = [(item, j), False]
+            st.p[t] = [(item, j), False, 2 if kind == "write_p" else 1]
+        elif kind == "write_p_half":
+            t, item, j = op[1:4]
+            if st.p[t][0] != (item, j) or st.p[t][2] != 1:
+                raise Violation(f"softmax {t} writes the second half of P({item},{j}) over {st.p[t]}")
+            st.p[t][2] = 2
         elif kind == "read_o":
             _, t, item = op
             if st.o_item[t] != item or st.o_done_n[t] != self._nk(item, t):
