@@ -123,8 +123,8 @@ def load_timeline_library():
 
 def debug_timeline(lib, reset: bool = True) -> np.ndarray:
     """The role timeline of the last call made through ``lib`` (the debug
-    library): uint64 clock64 stamps [4, 64, 8], layout as in fp8attn.h."""
-    buf = np.zeros((4, 64, 8), dtype=np.uint64)
+    library): uint64 clock64 stamps [6, 64, 8], layout as in fp8attn.h."""
+    buf = np.zeros((6, 64, 8), dtype=np.uint64)
     st = lib.attn_debug_timeline(buf.ctypes.data, buf.size, int(bool(reset)))
     _raise(st, "attn_debug_timeline")
     return buf

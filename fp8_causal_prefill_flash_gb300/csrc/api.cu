@@ -77,15 +77,15 @@ int device_check(int* sms) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 4-D tensor map over a BSHD tensor: dims (D, H, S, B) innermost first; the
-// box is `box_inner` elements of D, one head, 128 rows of S, one batch.
+// box is `box_inner` elements of D, one head, `box_rows` rows of S, one batch.
 int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int D, int H,
-             int S, int B, int box_inner, CUtensorMapSwizzle sw) {
+             int S, int B, int box_inner, CUtensorMapSwizzle sw, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return ATTN_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize,
                            (cuuint64_t)S * H * D * esize};
-  cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, 128, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_inner, 1, (cuuint32_t)box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -203,6 +203,14 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   } else {
     maps.q64 = maps.q128;
     maps.k64 = maps.k128;
+  }
+  // bf16 output of the FP8 paths: TMA stores in boxes of 64 columns x 32 rows
+  if (fp8 && out_dtype == ATTN_OUT_BF16) {
+    if ((st = make_map(&maps.o64, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Dv, Hq, S, B, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B, 32)))
+      return st;
+  } else {
+    maps.o64 = maps.v;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (variant) {
@@ -327,7 +335,7 @@ int attn_api_version(void) { return FP8ATTN_API_VERSION; }
 
 int attn_debug_timeline(unsigned long long* host, int capacity, int reset) {
 #ifdef FA8_TIMELINE
-  constexpr int kN = 4 * 64 * 8;
+  constexpr int kN = 6 * 64 * 8;
   if (!host || capacity < 0) return ATTN_ERR_INVALID_ARG;
   int sms = 0;
   const int st = device_check(&sms);

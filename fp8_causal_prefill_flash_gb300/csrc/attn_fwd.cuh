@@ -67,9 +67,11 @@
 namespace fa8 {
 
 // Optional role timeline (debug builds with -DFA8_TIMELINE): clock64 stamps of
-// CTA 0's first item, one row of stamps per key tile, written to fa8_timeline.
+// CTA 0, written to fa8_timeline.  Roles 0-3: the first item, one row of
+// stamps per key tile.  Roles 4-5: one row per item (round) of CTA 0, the
+// events at the items' boundaries.
 #ifdef FA8_TIMELINE
-__device__ unsigned long long fa8_timeline[4][64][8];
+__device__ unsigned long long fa8_timeline[6][64][8];
 #define FA8_TL(role, j, k)                                                    \
   do {                                                                        \
     if (blockIdx.x == 0 && (j) < 64) fa8_timeline[role][j][k] = clock64();    \
@@ -131,7 +133,17 @@ struct Cfg {
   // B operand, so that O's column 128 accumulates the rounded row sum
   static constexpr int kOnesBytes = kBlockScaled ? 128 * 128 : 0;
   static constexpr int kSmemOnes = kSmemV + kStages * kVTileBytes;
-  static constexpr int kSmemBytes = kSmemOnes + kOnesBytes;
+  // bf16 output through TMA stores: one 4 KB slot per softmax warp, 32 rows x
+  // 64 columns in the 128-byte swizzle, stored in two halves, so that the
+  // softmax warps do not wait for the scattered 16-byte row stores of the
+  // BSHD layout at an item's end.  Measured against direct stores in one
+  // session: Lean-P 2-8% faster from 2K to 8K keys and even at 16K-32K; the
+  // other paths' softmax code compiled slower with it (the ablation by 13%),
+  // so they keep direct stores.
+  static constexpr bool kEpiTma = V == kLeanP;
+  static constexpr int kOutSlotBytes = 32 * 128;
+  static constexpr int kSmemOut = kSmemOnes + kOnesBytes;  // a multiple of 1024
+  static constexpr int kSmemBytes = kSmemOut + (kEpiTma ? 8 * kOutSlotBytes : 0);
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
   static constexpr int kQkSteps = kRowBytes / 32;       // one MMA per 32 bytes of K
   static constexpr int kPvSteps = kFp8 ? 4 : 8;         // 128 keys / (32 fp8 or 16 bf16)
@@ -148,6 +160,10 @@ struct Cfg {
   // (running-maximum anchor) faster at the MLA shape, where the S product is
   // six MMAs, but 1-3% slower at head dim 128 and slower on the exact paths.
   static constexpr bool kPHalves = DQK == 192 && (V == kLeanP || V == kLeanPA3);
+  // epilogue: all of O_t read with one wait and O_t released before the
+  // output stores (FP8 paths; the BF16 softmax, short of registers already,
+  // measured 12% slower with the 128-column read)
+  static constexpr bool kEarlyOFree = kFp8;
   // tensor-memory columns
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColP0 = 128, kColP1 = kFp8 ? 176 : 192;
@@ -155,6 +171,7 @@ struct Cfg {
   static constexpr uint32_t kColO0 = kFp8 ? 224 : 256, kColO1 = kFp8 ? 368 : 384;
   static_assert(kTailBytes == 0 || kTailBytes == 64, "row bytes must be 128*n or 128*n+64");
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+  static_assert(kSmemOut % 1024 == 0, "128-byte swizzled slots need 1024-byte alignment");
 };
 
 struct KParams {
@@ -181,6 +198,7 @@ struct KParams {
 struct Maps {
   CUtensorMap q128, k128, v;  // 128-byte panels (SW128)
   CUtensorMap q64, k64;       // 64-byte tail panel of the MLA shape (SW64)
+  CUtensorMap o64;            // bf16 output, boxes of 64 columns x 32 rows (SW128)
 };
 
 // Items are visited longest first (query block descending); CTA c takes the
@@ -269,6 +287,7 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
     const uint32_t qbuf = q_it % C::kQBufs, qph = (q_it / C::kQBufs) & 1;
     if (!mbar_wait(&bars.q_empty[qbuf], qph ^ 1, ab, p.wait_limit_ns)) break;
     uint8_t* qdst = smem + C::kSmemQ + qbuf * C::kQBufBytes;
+    FA8_TL(4, round, 0);
     mbar_arrive_expect_tx(&bars.q_full[qbuf], 2 * C::kQkTileBytes);
     load_qk_tile<V, DQK>(qdst, m, true, &bars.q_full[qbuf], h, qb * 256, b);
     load_qk_tile<V, DQK>(qdst + C::kQkTileBytes, m, true, &bars.q_full[qbuf], h, qb * 256 + 128,
@@ -281,6 +300,7 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
       mbar_arrive_expect_tx(&bars.k_full[st], C::kQkTileBytes);
       load_qk_tile<V, DQK>(smem + C::kSmemK + st * C::kQkTileBytes, m, false, &bars.k_full[st], g,
                            j * kBN, b);
+      if (j == 0) FA8_TL(4, round, 1);
       ++nk;
       if (!mbar_wait(&bars.v_empty[st], ph ^ 1, ab, p.wait_limit_ns)) break;
       ++nv;
@@ -391,6 +411,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
     const uint32_t qbuf = q_it % C::kQBufs;
     const uint32_t q_buf_off = C::kSmemQ + qbuf * C::kQBufBytes;
     if (!mbar_wait(&bars.q_full[qbuf], (q_it / C::kQBufs) & 1, ab, lim)) return;
+    FA8_TL(4, round, 2);
     ++q_it;
     for (int j = 0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
@@ -409,11 +430,13 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 3]);
         tc_commit(&bars.s_full[t]);
         if (stamp) FA8_TL(2 + t, j, 5);
+        if (j == 0 && t == 0) FA8_TL(4, round, 3);
         ++issued[t];
         last = t;
       }
       tc_commit(&bars.k_empty[st]);
     }
+    FA8_TL(4, round, 4);
     tc_commit(&bars.q_empty[qbuf]);
   }
 }
@@ -480,9 +503,11 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         ++p_cnt[t];
         tc_commit(&bars.o_done[t]);
         if (stamp) FA8_TL(2 + t, j, 2);
+        if (j == 0 && t == 0) FA8_TL(4, round, 5);
       }
       tc_commit(&bars.v_empty[st]);
     }
+    FA8_TL(4, round, 6);
     qk_base[0] += nk0;
     qk_base[1] += nkv;
     ++items;
@@ -553,7 +578,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int V, int DQK>
-__device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, int t) {
+__device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, Barriers& bars,
+                             uint32_t tmem, int t) {
   using C = Cfg<V, DQK>;
   volatile int* ab = &bars.abort_flag;
   const uint64_t lim = p.wait_limit_ns;
@@ -592,6 +618,7 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
       if (stamp) FA8_TL(t, j, 0);
       if (!warp_wait(&bars.s_full[t], s_cnt & 1, ab, lim)) return;
       if (stamp) FA8_TL(t, j, 1);
+      if (j == 0 && r == 0) FA8_TL(5, round, 4 * t);
       ++s_cnt;
       tc_fence_after();
       uint32_t s[128];
@@ -815,33 +842,71 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
     }
     // epilogue: out = dv * O / l
     if (!warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return;
+    if (r == 0) FA8_TL(5, round, 4 * t + 1);
     tc_fence_after();
-    if constexpr (C::kBlockScaled) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
-    const float inv = dvv / l;
-    // log-sum-exp of the row in natural units: the row sum l is relative to
-    // 2^ref (Lean-P: the scaled rounded weights; exact paths: the unrounded p)
-    // the reference in log2 units (the A3 path keeps it in raw-score units)
-    const float ref2 = V == kLeanPA3 ? ref * lam : ref;
-    if (p.lse && row < p.S)
-      p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
     const bool store = row < p.S;
     const size_t orow = ((size_t)b * p.S + (size_t)(row < p.S ? row : 0)) * p.Hq + h;
-#pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-      uint32_t o[32];
-      tmem_ld32_wait(o_col + c, o);
-      if (store) {
-        if (p.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV + c);
+    // the reference in log2 units (the A3 path keeps it in raw-score units)
+    const float ref2 = V == kLeanPA3 ? ref * lam : ref;
+    // row sum l (relative to 2^ref): Lean-P paths, the scaled rounded weights
+    // in O's row-sum column; exact paths, the unrounded p summed on the cores
+    if constexpr (C::kEarlyOFree) {
+      // O_t (and its row-sum column) in registers with one wait, then O_t is
+      // released before the stores, so the next item's first P.V product
+      // does not wait for them
+      uint32_t o[128];
+      uint32_t lsum;
+      tmem_ld128_1_wait(o_col, o_col + (C::kBlockScaled ? 128 : 0), o, lsum);
+      tc_fence_before();
+      mbar_arrive(&bars.o_free[t]);
+      if (r == 0) FA8_TL(5, round, 4 * t + 2);
+      if constexpr (C::kBlockScaled) l = __uint_as_float(lsum);
+      const float inv = dvv / l;
+      if (p.lse && store)
+        p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
+      if (C::kEpiTma && !p.out_f32) {
+        // bf16 rows through this warp's shared-memory slot and TMA stores (the
+        // tensor map clips rows past S): the warp does not wait for global
+        // memory, only for the slot's previous contents to have been read
+        uint8_t* slot = smem + C::kSmemOut + (t * 4 + quad) * C::kOutSlotBytes;
+        const int row0 = qb * 256 + t * 128 + (int)quad * 32;
+        const uint32_t lane = lane_id();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
+        for (int half = 0; half < 2; ++half) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // 16-byte chunk c: columns 64*half + 8c .. +7
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int col = 64 * half + 8 * c + 2 * k;
+              __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(o[col]) * inv,
+                                                        __uint_as_float(o[col + 1]) * inv);
+              w[k] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            *reinterpret_cast<uint4*>(slot + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < p.S) {  // a box wholly past S stores nothing
+            tma_store_4d(&maps.o64, slot, 64 * half, h, row0, b);
+            bulk_commit();
+          }
+        }
+      } else if (store) {
+        if (p.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
             dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
                                  __uint_as_float(o[4 * i + 2]) * inv,
                                  __uint_as_float(o[4 * i + 3]) * inv);
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV + c);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 16; ++i) {
             uint32_t w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -853,9 +918,43 @@ __device__ void softmax_loop(const KParams& p, Barriers& bars, uint32_t tmem, in
           }
         }
       }
+      if (r == 0) FA8_TL(5, round, 4 * t + 3);
+    } else {
+      if constexpr (C::kBlockScaled) l = __uint_as_float(tmem_ld1_wait(o_col + 128));
+      const float inv = dvv / l;
+      if (p.lse && store)
+        p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
+#pragma unroll 1
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t o[32];
+        tmem_ld32_wait(o_col + c, o);
+        if (store) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                   __uint_as_float(o[4 * i + 2]) * inv,
+                                   __uint_as_float(o[4 * i + 3]) * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(o[8 * i + 2 * k]) * inv,
+                                                          __uint_as_float(o[8 * i + 2 * k + 1]) * inv);
+                w[k] = *reinterpret_cast<uint32_t*>(&hv);
+              }
+              dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.o_free[t]);
     }
-    tc_fence_before();
-    mbar_arrive(&bars.o_free[t]);
   }
 }
 
@@ -924,7 +1023,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp < 8) {
-    softmax_loop<V, DQK>(p, bars, tmem, warp / 4);
+    softmax_loop<V, DQK>(p, maps, smem, bars, tmem, warp / 4);
+    // bulk stores of the output must be complete before the CTA exits
+    if (C::kEpiTma && lane_id() == 0) bulk_wait_all();
+    __syncwarp();
   } else if (warp == kProducerWarp) {
     producer_loop<V, DQK>(p, maps, smem, bars);
   } else if (warp == kQkWarp || warp == kPvWarp) {

@@ -72,7 +72,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 6
+#define FP8ATTN_API_VERSION 7
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -239,13 +239,20 @@ int attn_api_version(void);
 
 /* Debug timeline (only in the debug library built with FA8_TIMELINE; the
  * release library returns ATTN_ERR_UNSUPPORTED without touching the device).
- * Copies the clock64 stamps that CTA 0 recorded for its first work item into
- * host[0 .. min(capacity, 2048)), as [4][64][8] unsigned 64-bit values:
+ * Copies the clock64 stamps that CTA 0 recorded into
+ * host[0 .. min(capacity, 3072)), as [6][64][8] unsigned 64-bit values.  Its
+ * first work item, per key tile j:
  *   [t][j][0..4]   softmax of query tile t, key tile j: before the wait for S,
  *                  S ready, S copied out (arrived), codes computed, P stored
  *   [2+t][j][0..2] P.V issuer for tile t: before the wait for P, P ready, P.V
  *                  issued;  [2+t][j][3..5] S issuer for tile t: before the
  *                  wait for S to be free, S free, S product issued
+ * Every item (round r of CTA 0), at its boundaries:
+ *   [4][r][0..6]   Q load issued, first K load issued, Q ready for the S
+ *                  issuer, first S product issued, last S product issued,
+ *                  first P.V product issued, last P.V product issued
+ *   [5][r][4t+0..3] softmax of tile t: first S ready, last P.V complete
+ *                  (epilogue start), O released, output stored
  * Unwritten entries are 0 (after a reset) or hold older launches' stamps.
  * With reset != 0 the device copy is zeroed afterwards.  Synchronous with
  * respect to the device; for profiling, not for production calls. */

@@ -25,7 +25,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 6
+    assert lib.attn_api_version() == 7
     assert lib.attn_launches_per_call() == 1
 
 
