@@ -33,6 +33,14 @@
 // "How does ZYFA work?"): asynchronous tcgen05 MMAs tracked by mbarriers
 // provide the overlap.
 //
+// At the MLA shape the Lean-P paths write P in two 64-key halves, and the P.V
+// warp issues each product's first two K-steps as soon as the first half is in
+// tensor memory (Cfg::kPHalves).  An item ends with its epilogue in the
+// softmax warps: out = dv * O / l, O read with one wait and released before
+// the output is written; the Lean-P path writes bf16 rows into a 4 KB
+// shared-memory slot per warp and stores them with TMA (Cfg::kEpiTma), so that
+// the next item's first S product does not wait for scattered row stores.
+//
 // Probability policies (softmax warpgroups):
 //   kLeanP     one saturating multiply-add per probability rounded toward
 //              minus infinity, whose value floored to 1/128 is the e4m3 code,
@@ -137,7 +145,7 @@ struct Cfg {
   // 64 columns in the 128-byte swizzle, stored in two halves, so that the
   // softmax warps do not wait for the scattered 16-byte row stores of the
   // BSHD layout at an item's end.  Measured against direct stores in one
-  // session: Lean-P 2-8% faster from 2K to 8K keys and even at 16K-32K; the
+  // session: Lean-P 2-8% faster from 2K to 8K keys and level at 16K-32K; the
   // other paths' softmax code compiled slower with it (the ablation by 13%),
   // so they keep direct stores.
   static constexpr bool kEpiTma = V == kLeanP;
