@@ -535,8 +535,10 @@ def run_ours(args, rank, world, local_rank):
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak_fp8,
                          "unit": "TFLOP/s", "frac": per_gpu / peak_fp8,
                          "traffic": args.traffic if args.traffic is not None else profiled_traffic(),
-                         "peak_note": (f"{peaks['source']} bf16 burst {peaks['bf16_burst']} "
-                                       f"TFLOP/s x {FP8_OVER_BF16} (nominal FP8:BF16)")},
+                         "peak_note": (f"derived, not an FP8 measurement: {peaks['source']} bf16 "
+                                       f"burst {peaks['bf16_burst']} TFLOP/s x {FP8_OVER_BF16} "
+                                       f"(nominal FP8:BF16); clock-aware fractions in "
+                                       f"frac_clock_aware")},
             "e2e": {"value": job_tflops(F, world, ms_e2e), "unit": "TFLOP/s",
                     "ms_per_step": ms_e2e, "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h),
@@ -630,7 +632,8 @@ def extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms, n):
         legs[key] = {"workload": name, "value": tf, "unit": "TFLOP/s", "ms_per_step": ms,
                      "steps": n, "peak": peak, "frac": tf / peak,
                      "peak_note": f"{peaks['source']} bf16 burst"
-                                  + (f" x {FP8_OVER_BF16}" if kind == "fp8" else ""),
+                                  + (f" x {FP8_OVER_BF16} (derived: nominal FP8:BF16)"
+                                     if kind == "fp8" else ""),
                      "frac_clock_aware": clock_normalised(tf, kind, peaks, sms,
                                                           clk.get("sm_mhz")),
                      "clocks": clk}

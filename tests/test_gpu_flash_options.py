@@ -152,3 +152,19 @@ def test_float8_tensors_and_binding_errors():
         fa.attn_fwd_fp8(q.cpu(), k, v, *d)                          # not on the GPU
     with pytest.raises(fa.AttnError):
         fa.attn_fwd_fp8(q[:, :, :3].contiguous(), k, v, *d)         # Hq % Hkv != 0
+
+
+def test_host_descales_are_checked():
+    """The descale contract (finite and greater than zero) at the binding:
+    host numbers are checked before any launch; device descales are the
+    caller's (fp8attn.h).  A valid host descale gives the device tensor's
+    result bit for bit."""
+    case = wl.fp8_gaussian_case(1, 2, 2, 130, 128, 128, seeds=(126, 127, 128))
+    q, k, v, d = _fp8_dev(case, case.dq, case.dk, case.dv)
+    for bad in (0.0, -case.dq, float("inf"), float("nan")):
+        with pytest.raises(ValueError):
+            fa.flash_attn_fp8_func(q, k, v, bad, d[1], d[2])
+    a = fa.flash_attn_fp8_func(q, k, v, float(d[0].item()), d[1], d[2])
+    b = fa.flash_attn_fp8_func(q, k, v, *d)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
