@@ -84,3 +84,21 @@ def test_energy_meter_and_report():
     # an unknown device or an unread counter gives no report, not an error
     assert bench.EnergyMeter("bad", nvml=_FakeNvml()).read_mj() is None
     assert bench.energy_report(None, 5, 1.0) is None and bench.energy_report(5, 5, 1.0) is None
+
+
+def test_clock_aware_fractions():
+    """The bench line's clock-aware denominators: the sustained bf16 GEMM scaled
+    from the clock it ran at to the kernel's clock (x2 for FP8), and the
+    tensor pipes' issue rate at the kernel's clock."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"bf16_sustained": 1700.0, "sustained_mhz": 1400.0}
+    r = bench.clock_normalised(2000.0, "fp8", peaks, 152, 2100.0)
+    assert abs(r["measured_sustained_at_kernel_clock"]["peak"] - 1700.0 * 2 * 1.5) < 1e-9
+    assert abs(r["mma_issue_rate_at_kernel_clock"]["peak"] - 16384 * 152 * 2100e6 / 1e12) < 1e-9
+    assert abs(r["mma_issue_rate_at_kernel_clock"]["frac"] * r["mma_issue_rate_at_kernel_clock"]["peak"]
+               - 2000.0) < 1e-9
+    b = bench.clock_normalised(1000.0, "bf16", peaks, 152, 2100.0)
+    assert abs(b["measured_sustained_at_kernel_clock"]["peak"] - 1700.0 * 1.5) < 1e-9
+    # no clock sampled: only the kernel clock (None) is reported
+    assert bench.clock_normalised(1000.0, "fp8", peaks, 152, None) == {"kernel_sm_mhz": None}
