@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3952270336,
-                    "sources_sha256": "15abc4694468fed0ff2b8c0a55488c79e233d5636cb638ca0ce9d1b812ac465a"}
+PROFILED_TRAFFIC = {"bytes": 3950085376,
+                    "sources_sha256": "eb12b3d7285e18f0b2216ee9fce8fe3948076aec741d75840fe8d3d8636326e0"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")
