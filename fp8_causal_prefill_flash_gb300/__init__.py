@@ -11,6 +11,9 @@ Entry points (same names as the C ABI):
 * ``attn_fwd_fp8_exact(...)`` -- exact-softmax FP8 ablation
 * ``attn_fwd_bf16(q, k, v)`` -- exact-softmax BF16
 * ``attn_fwd_ex(variant, ...)`` -- fp32 output, explicit scale, status word
+* ``attn_fwd_full(variant, ...)`` -- plus non-causal, per-(batch, kv head)
+  descales, LSE, and the split schedule for problems with few work items
+  (its workspace comes from torch's caching allocator on the call's stream)
 
 Tensors are [B, S, H, D] contiguous CUDA tensors: uint8 / float8_e4m3fn codes
 for FP8 (descales are one-element float32 CUDA tensors), bfloat16 for BF16.
@@ -70,7 +73,7 @@ def build(force: bool = False, timeline: bool = False) -> str:
 
 def _open(path):
     lib = ctypes.CDLL(path)
-    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     fp8_args = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]
     lib.attn_fwd_fp8.argtypes = fp8_args
     lib.attn_fwd_fp8_exact.argtypes = fp8_args
@@ -79,11 +82,12 @@ def _open(path):
                                 vp, vp]
     lib.attn_quantize_fp8.argtypes = [vp, i, vp, vp, i, i, i, i, i, vp]
     lib.attn_fwd_full.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
-                                  i, vp, vp]
+                                  i, vp, vp, sz, vp]
+    lib.attn_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(sz)]
     lib.attn_debug_timeline.argtypes = [vp, i, i]
     for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
                  "attn_quantize_fp8", "attn_fwd_full", "attn_launches_per_call",
-                 "attn_api_version", "attn_debug_timeline"):
+                 "attn_api_version", "attn_debug_timeline", "attn_workspace_size"):
         getattr(lib, name).restype = ctypes.c_int
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -289,11 +293,29 @@ def attn_quantize_fp8(x, hadamard=False, codes=None, descale=None):
     return codes, descale
 
 
+def workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal=True, flags=0) -> int:
+    """Bytes of workspace ``attn_fwd_full`` uses on the current device for
+    these arguments (``attn_workspace_size`` of the C ABI): 0 unless the
+    problem has too few work items to fill the SMs and the variant's codes
+    depend on each key block alone (Lean-P, block-exact)."""
+    n = ctypes.c_size_t(0)
+    st = load_library().attn_workspace_size(int(variant), B, Hq, Hkv, S, Dqk, Dv,
+                                            int(bool(causal)), int(flags), ctypes.byref(n))
+    _raise(st, "attn_workspace_size")
+    return int(n.value)
+
+
 def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None, out=None,
                   out_dtype=ATTN_OUT_BF16, causal=True, softmax_scale=None, return_lse=False,
-                  dev_status=None, flags=0):
+                  dev_status=None, flags=0, split=True, workspace=None):
     """The general entry point (``attn_fwd_full`` of the C ABI).  Descales are
     one-element tensors or [B, Hkv] tensors (one per batch and kv head).
+    With ``split`` (the default) a problem with too few work items to fill
+    the SMs splits its longest items along the keys; the workspace this needs
+    is ``workspace`` (a uint8 CUDA tensor of at least ``workspace_size``
+    bytes, used by one call at a time) or, by default, a new tensor from
+    torch's caching allocator, which keeps it for this call's stream until the
+    call's work is done.  ``split=False`` runs every item whole.
     Returns ``out``, or ``(out, lse)`` with lse fp32 [B, Hq, S] (natural log of
     the row's own unnormalised weights)."""
     lib = load_library()
@@ -311,10 +333,22 @@ def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=No
     dtype = torch.float32 if out_dtype == ATTN_OUT_F32 else torch.bfloat16
     out = _out(out, q, Dv, dtype)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if return_lse else None
+    stream = _stream_handle(q)
+    ws, ws_bytes = None, 0
+    if split:
+        need = workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal, flags)
+        if need:
+            if workspace is None:
+                workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            elif (not workspace.is_cuda or workspace.dtype != torch.uint8 or
+                  workspace.numel() < need or not workspace.is_contiguous()):
+                raise ValueError(f"workspace must be a contiguous uint8 CUDA tensor of at least "
+                                 f"{need} bytes")
+            ws, ws_bytes = workspace, int(workspace.numel())
     st = lib.attn_fwd_full(variant, _ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
                            _ptr(descale_v), _ptr(out), out_dtype, _ptr(lse), B, Hq, Hkv, S, Dqk,
                            Dv, int(bool(causal)), float(softmax_scale or 0.0), flags,
-                           _ptr(dev_status), _stream_handle(q))
+                           _ptr(dev_status), _ptr(ws), ws_bytes, stream)
     _raise(st, "attn_fwd_full")
     return (out, lse) if return_lse else out
 

@@ -8,6 +8,8 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <random>
+#include <vector>
 
 #include "../../include/fp8attn.h"
 #include "attn_fwd.cuh"
@@ -26,6 +28,10 @@ constexpr int kMaxDevices = 64;
 // that the two or three chunks' worth of kv heads in flight stay in L2.
 constexpr size_t kChunkAllBytes = 256ull << 20;
 constexpr size_t kChunkBytes = 64ull << 20;
+// Split schedule: considered for problems with fewer than kSplitMaxWaves * SMs
+// items, with a workspace of at most kSplitMaxBytes.
+constexpr int kSplitMaxWaves = 4;
+constexpr size_t kSplitMaxBytes = 128ull << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -93,10 +99,10 @@ int make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT = false>
 int launch(const Maps& maps, const KParams& p, int sms, cudaStream_t stream) {
   using C = fa8::Cfg<V, DQK>;
-  auto kern = fa8::attn_fwd_kernel<V, DQK>;
+  auto kern = fa8::attn_fwd_kernel<V, DQK, SPLIT>;
   // Per-device opt-in to the large dynamic shared memory carve-out.
   static std::atomic<unsigned long long> done_mask[1] = {0};
   int dev = 0;
@@ -108,15 +114,133 @@ int launch(const Maps& maps, const KParams& p, int sms, cudaStream_t stream) {
       return ATTN_ERR_CUDA;
     done_mask[0].fetch_or(bit, std::memory_order_acq_rel);
   }
-  const int grid = p.n_items < sms ? p.n_items : sms;
+  const int grid = p.n_units < sms ? p.n_units : sms;
   kern<<<grid, fa8::kThreads, C::kSmemAlloc, stream>>>(maps, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- split plan
+struct SplitPlan {
+  int split_qb = 0, ns = 1, n_split_items = 0;
+  size_t ws_bytes = 0;
+};
+
+size_t split_ws_bytes(int n_split_items, int ns) {
+  return fa8::split_cnt_bytes(n_split_items) +
+         (size_t)n_split_items * ns * 2 * fa8::kSplitSlotFloats * sizeof(float);
+}
+
+// Estimated finishing time of the busiest CTA (ns) when the items of query
+// block >= sq are split into ns pieces (ns = 1: no split), following the
+// kernel's unit order and its alternating round-robin assignment (item_at):
+// per key tile of both query tiles `step`, per unit `unit_cost` (the item
+// boundary), per piece `piece_cost` (its partial result written, and the ns
+// partial results read and added up by the last piece).  The constants are a
+// least-squares fit to GB300 times of 100 forced plans (2 to 16 heads, 2K to
+// 8K keys, head dims 128 and 192; the model's time is within 10% of each).
+long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal, int Dqk, int sq,
+                         int ns, int grid, std::vector<long long>& load) {
+  const long long step = Dqk == 192 ? 1140 : 950, unit_cost = 5000;
+  const long long piece_cost = 3000 + 1000 * ns;
+  load.assign(grid, 0);
+  long long pos = 0;
+  auto place = [&](long long cost) {
+    const long long round = pos / grid, k = pos % grid;
+    const long long c = (round & 1) ? grid - 1 - k : k;
+    load[c] += cost + unit_cost;
+    ++pos;
+  };
+  auto nkv_of = [&](int qb) {
+    const int need = 2 * qb + 2;
+    return causal && need < n_kv_tiles ? need : n_kv_tiles;
+  };
+  if (ns > 1)
+    for (int qb = n_qblocks - 1; qb >= sq; --qb) {
+      const int n = nkv_of(qb);
+      for (int u = 0; u < units_bh; ++u)
+        for (int s = 0; s < ns; ++s)
+          place(((long long)(s + 1) * n / ns - (long long)s * n / ns) * step + piece_cost);
+    }
+  for (int qb = (ns > 1 ? sq : n_qblocks) - 1; qb >= 0; --qb) {
+    const long long n = nkv_of(qb);
+    for (int u = 0; u < units_bh; ++u) place(n * step);
+  }
+  long long m = 0;
+  for (long long x : load) m = x > m ? x : m;
+  return m;
+}
+
+// The split schedule for a problem (none unless it helps by 5% or more in the
+// model above: smaller predicted gains are within the model's error).  Plans
+// are cached: the search walks every candidate.
+SplitPlan split_plan(int units_bh, int S, int causal, int Dqk, int sms, size_t limit) {
+  SplitPlan best;
+  const int n_qblocks = (S + 255) / 256, n_kv_tiles = (S + 127) / 128;
+  const long long n_items = (long long)units_bh * n_qblocks;
+  if (n_items >= (long long)kSplitMaxWaves * sms) return best;
+  struct Entry {
+    int units_bh, S, causal, Dqk, sms;
+    size_t limit;
+    SplitPlan plan;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry& e : cache)
+      if (e.units_bh == units_bh && e.S == S && e.causal == causal && e.Dqk == Dqk &&
+          e.sms == sms && e.limit == limit)
+        return e.plan;
+  }
+  std::vector<long long> load;
+  const int grid0 = (int)(n_items < sms ? n_items : sms);
+  const long long base =
+      split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, Dqk, 0, 1, grid0, load);
+  long long best_t = base;
+  for (int ns = 2; ns <= 4; ++ns)
+    for (int sq = n_qblocks - 1; sq >= 0; --sq) {
+      const int nkv_min = causal && 2 * sq + 2 < n_kv_tiles ? 2 * sq + 2 : n_kv_tiles;
+      if (nkv_min < 2 * ns) break;  // every piece needs two key tiles
+      const int n_split = units_bh * (n_qblocks - sq);
+      const size_t bytes = split_ws_bytes(n_split, ns);
+      if (bytes > limit) break;
+      const long long n_units = n_items + (long long)n_split * (ns - 1);
+      const int grid = (int)(n_units < sms ? n_units : sms);
+      const long long t =
+          split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, Dqk, sq, ns, grid, load);
+      if (t < best_t) {
+        best_t = t;
+        best.split_qb = sq;
+        best.ns = ns;
+        best.n_split_items = n_split;
+        best.ws_bytes = bytes;
+      }
+    }
+  if (best.n_split_items > 0 && best_t * 100 > base * 95) best = SplitPlan();
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache.size() >= 64) cache.erase(cache.begin());
+  cache.push_back({units_bh, S, causal, Dqk, sms, limit, best});
+  return best;
+}
+
+// A tag per call that uses a split workspace (see split_arrive): distinct
+// across calls and, from a random start, across library copies in a process.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> epoch{[] {
+    std::random_device rd;
+    return ((((unsigned long long)rd() << 32) ^ rd()) & ((1ull << 58) - 1)) + 1;
+  }()};
+  return epoch.fetch_add(1, std::memory_order_relaxed) & ((1ull << 61) - 1);
+}
+
+bool split_variant(int variant) {
+  return variant == ATTN_VARIANT_LEANP || variant == ATTN_VARIANT_BLOCK_EXACT;
 }
 
 int run(int variant, const void* q, const void* k, const void* v, const float* dq, const float* dk,
         const float* dv, void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S,
         int Dqk, int Dv, int causal, float softmax_scale, int flags, int* dev_status,
-        void* stream) {
+        void* workspace, size_t workspace_bytes, void* stream) {
   // ---- argument checks (before anything touches the device)
   if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_LEANP_A3) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
@@ -136,6 +260,7 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
     return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
   if (Dv != 128) return ATTN_ERR_UNSUPPORTED;
   if (fp8 ? (Dqk != 128 && Dqk != 192) : (Dqk != 128)) return ATTN_ERR_UNSUPPORTED;
   // index ranges: the kernel's int arithmetic covers B*Hq*ceil(S/256) items
@@ -184,6 +309,19 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   p.causal = causal;
   p.descale_per_bkv = (flags & ATTN_FLAG_DESCALE_PER_BKV) ? 1 : 0;
   p.lse = lse;
+  // Split schedule: with a workspace, for the paths whose codes depend on each
+  // key block alone, in the plain (unchunked) item order.
+  SplitPlan plan;
+  if (workspace && split_variant(variant) && p.chunk_q == B * Hq)
+    plan = split_plan(B * Hq, S, causal, Dqk, sms, kSplitMaxBytes);
+  if (plan.n_split_items > 0 && workspace_bytes < plan.ws_bytes) return ATTN_ERR_INVALID_ARG;
+  p.split_qb = plan.split_qb;
+  p.split_ns = plan.ns;
+  p.n_split_items = plan.n_split_items;
+  p.n_units = (int)(n_items + (long long)plan.n_split_items * (plan.ns - 1));
+  p.ws = plan.n_split_items > 0 ? static_cast<unsigned char*>(workspace) : nullptr;
+  p.epoch = plan.n_split_items > 0 ? next_epoch() : 0;
+  const bool split = plan.n_split_items > 0;
 
   Maps maps;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -213,6 +351,13 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
     maps.o64 = maps.v;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (split) {
+    if (variant == ATTN_VARIANT_LEANP)
+      return Dqk == 128 ? launch<fa8::kLeanP, 128, true>(maps, p, sms, s)
+                        : launch<fa8::kLeanP, 192, true>(maps, p, sms, s);
+    return Dqk == 128 ? launch<fa8::kBlockExact, 128, true>(maps, p, sms, s)
+                      : launch<fa8::kBlockExact, 192, true>(maps, p, sms, s);
+  }
   switch (variant) {
     case ATTN_VARIANT_LEANP:
       return Dqk == 128 ? launch<fa8::kLeanP, 128>(maps, p, sms, s)
@@ -239,20 +384,21 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* desca
                  const float* descale_k, const float* descale_v, void* out, int B, int Hq,
                  int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
   return run(ATTN_VARIANT_LEANP, q, k, v, descale_q, descale_k, descale_v, out, ATTN_OUT_BF16,
-             nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+             nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, nullptr, 0, stream);
 }
 
 int attn_fwd_fp8_exact(const void* q, const void* k, const void* v, const float* descale_q,
                        const float* descale_k, const float* descale_v, void* out, int B,
                        int Hq, int Hkv, int S, int Dqk, int Dv, int causal, void* stream) {
   return run(ATTN_VARIANT_EXACT_FP8, q, k, v, descale_q, descale_k, descale_v, out,
-             ATTN_OUT_BF16, nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+             ATTN_OUT_BF16, nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, nullptr, 0,
+             stream);
 }
 
 int attn_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                   int S, int Dqk, int Dv, int causal, void* stream) {
   return run(ATTN_VARIANT_BF16, q, k, v, nullptr, nullptr, nullptr, out, ATTN_OUT_BF16, nullptr,
-             B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, stream);
+             B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, nullptr, 0, stream);
 }
 
 int attn_fwd_ex(int variant, const void* q, const void* k, const void* v, const float* descale_q,
@@ -260,16 +406,38 @@ int attn_fwd_ex(int variant, const void* q, const void* k, const void* v, const 
                 int Hq, int Hkv, int S, int Dqk, int Dv, int causal, float softmax_scale,
                 int flags, int* dev_status, void* stream) {
   return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, nullptr, B, Hq,
-             Hkv, S, Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
+             Hkv, S, Dqk, Dv, causal, softmax_scale, flags, dev_status, nullptr, 0, stream);
 }
 
 int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
                   const float* descale_q, const float* descale_k, const float* descale_v,
                   void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S, int Dqk,
                   int Dv, int causal, float softmax_scale, int flags, int* dev_status,
-                  void* stream) {
+                  void* workspace, size_t workspace_bytes, void* stream) {
   return run(variant, q, k, v, descale_q, descale_k, descale_v, out, out_dtype, lse, B, Hq, Hkv,
-             S, Dqk, Dv, causal, softmax_scale, flags, dev_status, stream);
+             S, Dqk, Dv, causal, softmax_scale, flags, dev_status, workspace, workspace_bytes,
+             stream);
+}
+
+int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                        int flags, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_LEANP_A3) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Dqk < 1 || Dv < 1 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  const long long n_items = (long long)B * Hq * ((S + 255) / 256);
+  if (n_items > (1ll << 30) || (long long)B * S > (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  if (!split_variant(variant) || (flags & ATTN_FLAG_TEST_CHUNK_UNITS)) return ATTN_OK;
+  // only the unchunked item order splits (see run)
+  const size_t kv_unit = (size_t)S * (size_t)(Dqk + Dv);
+  if (kv_unit * (size_t)((long long)B * Hkv) > kChunkAllBytes) return ATTN_OK;
+  int sms = 0;
+  const int st = device_check(&sms);
+  if (st != ATTN_OK) return st;
+  *bytes = split_plan(B * Hq, S, causal, Dqk, sms, kSplitMaxBytes).ws_bytes;
+  return ATTN_OK;
 }
 
 const char* attn_status_string(int status) {

@@ -3,8 +3,11 @@
 // One persistent CTA per SM.  A work item is (batch b, query head h, query
 // block qb) with two 128-row query tiles (rows 256*qb .. 256*qb+255); the two
 // tiles share every K/V tile that TMA brings in.  Items run longest first
-// (see decode_item for the chunked order of very large problems).  Roles (12
-// warps):
+// (see decode_item for the chunked order of very large problems).  Problems
+// with too few items to keep every SM busy run through the SPLIT kernels,
+// where the longest items are split along the keys into pieces that run on
+// different CTAs and are added up by the piece that finishes last (see
+// decode_unit and split_arrive).  Roles (12 warps):
 //   warps 0-3   softmax of query tile 0 (thread = row)
 //   warps 4-7   softmax of query tile 1
 //   warp  8     TMA producer: Q tiles once per item, K/V tiles through a ring
@@ -194,6 +197,7 @@ struct KParams {
   int n_qblocks;     // ceil(S / 256)
   int n_kv_tiles;    // ceil(S / 128)
   int n_items;       // B * Hq * n_qblocks
+  int n_units;       // work units: n_items, plus split_ns - 1 per split item
   const float* dq;   // device descales (FP8 only)
   const float* dk;
   const float* dv;
@@ -207,7 +211,21 @@ struct KParams {
   int causal;          // 1: keys j <= i; 0: all S keys
   int descale_per_bkv; // descales hold one value per (batch, kv head) instead of one
   float* lse;          // optional [B, Hq, S] natural-log row sums (nullptr: none)
+  // Split schedule (SPLIT kernels only): the items of query block >= split_qb,
+  // the first n_split_items of the plain order, run as split_ns pieces each.
+  int split_qb, split_ns, n_split_items;
+  unsigned char* ws;             // workspace: counters, then partial results
+  unsigned long long epoch;      // this call's tag in the counters (< 2^61)
 };
+
+// Split workspace layout: one 64-bit counter per (split item, query tile),
+// padded to 256 bytes, then one slot per (split item, piece, query tile) of
+// kSplitSlotFloats floats: O as [32 column quads][128 rows] float4, then the
+// row sums l[128] and the reference binades ref[128].
+constexpr int kSplitSlotFloats = 128 * 128 + 2 * 128;
+__host__ __device__ constexpr size_t split_cnt_bytes(int n_split_items) {
+  return ((size_t)n_split_items * 16 + 255) / 256 * 256;
+}
 
 struct Maps {
   CUtensorMap q128, k128, v;  // 128-byte panels (SW128)
@@ -249,6 +267,76 @@ __device__ __forceinline__ int kv_tiles_for(const KParams& p, int qb, int t) {
   return p.causal && need < p.n_kv_tiles ? need : p.n_kv_tiles;
 }
 
+// A work unit: a whole item, or (SPLIT kernels) one piece of a split item,
+// which covers key tiles [j0, end_t) of query tile t.
+struct Unit {
+  int u;          // unit index
+  int b, h, qb;
+  int j0, end0, end1;
+  int piece, ns;  // piece of ns (ns = 1: the whole item)
+  int sidx;       // split item index: its counters and partial results
+};
+
+// Unit u: with a split schedule the first n_split_items * split_ns units are
+// the pieces of the split items (consecutive pieces of one item), the rest the
+// other items in the plain order.  Piece s covers key tiles
+// [s*n/ns, (s+1)*n/ns) of the item's n; the schedule splits only items with
+// n >= 2*ns, so every piece gives both query tiles at least one key tile.
+template <bool SPLIT>
+__device__ __forceinline__ void decode_unit(const KParams& p, int u, Unit& w) {
+  int idx = u;
+  w.u = u;
+  w.piece = 0;
+  w.ns = 1;
+  w.sidx = 0;
+  if constexpr (SPLIT) {
+    const int n_split_units = p.n_split_items * p.split_ns;
+    if (u < n_split_units) {
+      w.sidx = u / p.split_ns;
+      w.piece = u - w.sidx * p.split_ns;
+      w.ns = p.split_ns;
+      idx = w.sidx;
+    } else {
+      idx = u - n_split_units + p.n_split_items;
+    }
+  }
+  decode_item(p, idx, w.b, w.h, w.qb);
+  w.j0 = 0;
+  w.end0 = kv_tiles_for(p, w.qb, 0);
+  w.end1 = kv_tiles_for(p, w.qb, 1);
+  if constexpr (SPLIT) {
+    if (w.ns > 1) {
+      const int n = w.end1;
+      w.j0 = w.piece * n / w.ns;
+      w.end1 = (w.piece + 1) * n / w.ns;
+      w.end0 = w.end0 < w.end1 ? w.end0 : w.end1;
+    }
+  }
+}
+
+// The arrival of one finished piece of split item sidx, query tile t, after
+// its partial result is in the workspace (and fenced): true for the piece
+// that arrives last.  The counter holds (epoch << 3) + pieces arrived; a
+// value with another epoch (an earlier call, or memory never used) counts as
+// zero, so the workspace needs no clearing between calls.
+__device__ __forceinline__ bool split_arrive(const KParams& p, int sidx, int ns, int t,
+                                             volatile int* ab) {
+  unsigned long long* cnt = reinterpret_cast<unsigned long long*>(p.ws) + (size_t)sidx * 2 + t;
+  unsigned long long old = atomicAdd(cnt, 0ull);
+  for (int it = 0;; ++it) {
+    const unsigned long long nw = (old >> 3) == p.epoch ? old + 1 : (p.epoch << 3) + 1;
+    const unsigned long long prev = atomicCAS(cnt, old, nw);
+    if (prev == old) break;
+    old = prev;
+    if (it > 64) {  // only the other pieces move the counter: a few retries at most
+      *ab = 1;
+      return false;
+    }
+  }
+  const unsigned long long before = (old >> 3) == p.epoch ? (old & 7ull) : 0ull;
+  return before == (unsigned long long)(ns - 1);
+}
+
 struct __align__(8) Barriers {
   uint64_t q_full[2], q_empty[2];  // per Q buffer
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
@@ -260,8 +348,10 @@ struct __align__(8) Barriers {
   uint64_t qk_go[2][4];   // S product n of tile t issued: qk_go[t][n % 4] (BF16)
   uint64_t o_free[2];     // softmax t has read O_t in its epilogue
   uint64_t drain[2];      // teardown: all MMAs of the QK / PV warp complete
+  uint64_t split_sync[2]; // SPLIT: the 128 threads of softmax t (a bounded group barrier)
   uint32_t tmem_base;
   int abort_flag;
+  int split_last[2];      // SPLIT: this query tile's piece arrived last
 };
 
 // --------------------------------------------------------------------------
@@ -282,7 +372,7 @@ __device__ __forceinline__ void load_qk_tile(uint8_t* dst, const Maps& m, bool i
   }
 }
 
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT>
 __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Barriers& bars) {
   using C = Cfg<V, DQK>;
   if (!elect_one()) return;
@@ -293,10 +383,11 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
   volatile int* ab = &bars.abort_flag;
   uint32_t kv_it = 0, q_it = 0, nk = 0, nv = 0;
   for (int round = 0;; ++round) {
-    const int idx = item_at(round, p.n_items);
-    if (idx < 0) break;
-    int b, h, qb;
-    decode_item(p, idx, b, h, qb);
+    const int u = item_at(round, p.n_units);
+    if (u < 0) break;
+    Unit w;
+    decode_unit<SPLIT>(p, u, w);
+    const int b = w.b, h = w.h, qb = w.qb;
     const int g = h / p.group;
     const uint32_t qbuf = q_it % C::kQBufs, qph = (q_it / C::kQBufs) & 1;
     if (!mbar_wait(&bars.q_empty[qbuf], qph ^ 1, ab, p.wait_limit_ns)) break;
@@ -307,14 +398,14 @@ __device__ void producer_loop(const KParams& p, const Maps& m, uint8_t* smem, Ba
     load_qk_tile<V, DQK>(qdst + C::kQkTileBytes, m, true, &bars.q_full[qbuf], h, qb * 256 + 128,
                          b);
     ++q_it;
-    const int nkv = kv_tiles_for(p, qb, 1);
-    for (int j = 0; j < nkv; ++j, ++kv_it) {
+    const int nkv = w.end1;
+    for (int j = w.j0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
       if (!mbar_wait(&bars.k_empty[st], ph ^ 1, ab, p.wait_limit_ns)) break;
       mbar_arrive_expect_tx(&bars.k_full[st], C::kQkTileBytes);
       load_qk_tile<V, DQK>(smem + C::kSmemK + st * C::kQkTileBytes, m, false, &bars.k_full[st], g,
                            j * kBN, b);
-      if (j == 0) FA8_TL(4, round, 1);
+      if (j == w.j0) FA8_TL(4, round, 1);
       ++nk;
       if (!mbar_wait(&bars.v_empty[st], ph ^ 1, ab, p.wait_limit_ns)) break;
       ++nv;
@@ -407,7 +498,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t smem_base, int 
 // QK warp: S = Q_t K_j^T in the order S0(0), S1(0), S0(1), S1(1), ... (tile 0
 // skips key tiles past its diagonal).  Each product waits until the previous
 // owner of S has copied it out.
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT>
 __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
   using C = Cfg<V, DQK>;
   if (lane_id() != 0) return;
@@ -417,17 +508,17 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
   uint32_t issued[2] = {0, 0};  // S products issued per tile
   int last = -1;                // tile of the previous S product
   for (int round = 0;; ++round) {
-    const int idx = item_at(round, p.n_items);
-    if (idx < 0) break;
-    int b, h, qb;
-    decode_item(p, idx, b, h, qb);
-    const int nk0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
+    const int u = item_at(round, p.n_units);
+    if (u < 0) break;
+    Unit w;
+    decode_unit<SPLIT>(p, u, w);
+    const int nk0 = w.end0, nkv = w.end1;
     const uint32_t qbuf = q_it % C::kQBufs;
     const uint32_t q_buf_off = C::kSmemQ + qbuf * C::kQBufBytes;
     if (!mbar_wait(&bars.q_full[qbuf], (q_it / C::kQBufs) & 1, ab, lim)) return;
     FA8_TL(4, round, 2);
     ++q_it;
-    for (int j = 0; j < nkv; ++j, ++kv_it) {
+    for (int j = w.j0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
       if (!mbar_wait(&bars.k_full[st], ph, ab, lim)) return;
       for (int t = 0; t < 2; ++t) {
@@ -444,7 +535,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         if constexpr (C::kOrderPv) mbar_arrive(&bars.qk_go[t][issued[t] & 3]);
         tc_commit(&bars.s_full[t]);
         if (stamp) FA8_TL(2 + t, j, 5);
-        if (j == 0 && t == 0) FA8_TL(4, round, 3);
+        if (j == w.j0 && t == 0) FA8_TL(4, round, 3);
         ++issued[t];
         last = t;
       }
@@ -468,7 +559,7 @@ __device__ void qk_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
 // the P.V product that consumes n, which waits for that P.V product.  (With
 // two barriers this fails at an item's start, where P_t(0) is written without
 // waiting for any P.V product.)
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT>
 __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, uint32_t tmem) {
   using C = Cfg<V, DQK>;
   if (lane_id() != 0) return;
@@ -478,12 +569,12 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
   uint32_t qk_base[2] = {0, 0};  // S products of each tile in earlier items
   uint32_t go_seen[2] = {0, 0};  // qk_go arrivals consumed per tile
   for (int round = 0;; ++round) {
-    const int idx = item_at(round, p.n_items);
-    if (idx < 0) break;
-    int b, h, qb;
-    decode_item(p, idx, b, h, qb);
-    const int nk0 = kv_tiles_for(p, qb, 0), nkv = kv_tiles_for(p, qb, 1);
-    for (int j = 0; j < nkv; ++j, ++kv_it) {
+    const int u = item_at(round, p.n_units);
+    if (u < 0) break;
+    Unit w;
+    decode_unit<SPLIT>(p, u, w);
+    const int nk0 = w.end0, nkv = w.end1, j0 = w.j0;
+    for (int j = j0; j < nkv; ++j, ++kv_it) {
       const uint32_t st = kv_it % C::kStages, ph = (kv_it / C::kStages) & 1;
       const bool stamp = round == 0;
       if (!mbar_wait(&bars.v_full[st], ph, ab, lim)) return;
@@ -492,13 +583,13 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         if (stamp) FA8_TL(2 + t, j, 0);
         if (!mbar_wait(C::kPHalves ? &bars.p_half[t] : &bars.p_full[t], p_cnt[t] & 1, ab, lim))
           return;
-        if (j == 0) {
-          // the previous item's epilogue must have read O_t
+        if (j == j0) {
+          // the previous unit's epilogue must have read O_t
           if (!mbar_wait(&bars.o_free[t], (items & 1) ^ 1, ab, lim)) return;
         }
         if constexpr (C::kOrderPv) {
           const int nk = t ? nkv : nk0;
-          const uint32_t upto = qk_base[t] + (j + 1 < nk ? j + 1 : j);
+          const uint32_t upto = qk_base[t] + (j + 1 < nk ? j + 1 : j) - j0;
           for (; go_seen[t] <= upto; ++go_seen[t])
             if (!mbar_wait(&bars.qk_go[t][go_seen[t] & 3], (go_seen[t] >> 2) & 1, ab, lim))
               return;
@@ -507,23 +598,23 @@ __device__ void pv_loop(const KParams& p, uint32_t smem_base, Barriers& bars, ui
         tc_fence_after();
         const uint32_t v_off = C::kSmemV + st * C::kVTileBytes;
         if constexpr (C::kPHalves) {
-          issue_pv<V, DQK, 0, 2>(tmem, smem_base, t, v_off, j > 0);
+          issue_pv<V, DQK, 0, 2>(tmem, smem_base, t, v_off, j > j0);
           if (!mbar_wait(&bars.p_full[t], p_cnt[t] & 1, ab, lim)) return;
           tc_fence_after();
           issue_pv<V, DQK, 2, 4>(tmem, smem_base, t, v_off, true);
         } else {
-          issue_pv<V, DQK, 0, C::kPvSteps>(tmem, smem_base, t, v_off, j > 0);
+          issue_pv<V, DQK, 0, C::kPvSteps>(tmem, smem_base, t, v_off, j > j0);
         }
         ++p_cnt[t];
         tc_commit(&bars.o_done[t]);
         if (stamp) FA8_TL(2 + t, j, 2);
-        if (j == 0 && t == 0) FA8_TL(4, round, 5);
+        if (j == j0 && t == 0) FA8_TL(4, round, 5);
       }
       tc_commit(&bars.v_empty[st]);
     }
     FA8_TL(4, round, 6);
-    qk_base[0] += nk0;
-    qk_base[1] += nkv;
+    qk_base[0] += nk0 - j0;
+    qk_base[1] += nkv - j0;
     ++items;
   }
 }
@@ -591,7 +682,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT>
 __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, Barriers& bars,
                              uint32_t tmem, int t) {
   using C = Cfg<V, DQK>;
@@ -606,20 +697,21 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
   const float log2e = 1.4426950408889634f;
   const LeanPConsts kc = leanp_consts();
   uint32_t s_cnt = 0, o_cnt = 0;
+  uint32_t sync_cnt = 0;  // SPLIT: phases of split_sync[t] passed
   // The next item's coordinates and descales, worked out one item ahead
   // (kPrefetchItem): issued before the previous item's epilogue, the index
   // divisions and the descales' global-memory latency are not between that
   // epilogue and this item's first S hand-over.
-  int nb = 0, nh = 0, nqb = 0;
+  Unit nw{};
   bool nvalid = false;
   float dqk_next = 1.0f, dvv_next = 1.0f;
   auto prefetch_item = [&](int round_) {
-    const int idx_ = item_at(round_, p.n_items);
-    nvalid = idx_ >= 0;
+    const int u_ = item_at(round_, p.n_units);
+    nvalid = u_ >= 0;
     if (!nvalid) return;
-    decode_item(p, idx_, nb, nh, nqb);
+    decode_unit<SPLIT>(p, u_, nw);
     if constexpr (C::kFp8) {
-      const int di = p.descale_per_bkv ? nb * p.Hkv + nh / p.group : 0;
+      const int di = p.descale_per_bkv ? nw.b * p.Hkv + nw.h / p.group : 0;
       dqk_next = __ldg(p.dq + di) * __ldg(p.dk + di);
       dvv_next = __ldg(p.dv + di);
     }
@@ -627,23 +719,25 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
   if constexpr (C::kPrefetchItem) prefetch_item(0);
 
   for (int round = 0;; ++round) {
-    int b, h, qb;
+    Unit w;
     float dqk = 1.0f, dvv = 1.0f;  // descales of this (batch, kv head)
     if constexpr (C::kPrefetchItem) {
       if (!nvalid) break;
-      b = nb, h = nh, qb = nqb;
+      w = nw;
       dqk = dqk_next, dvv = dvv_next;
     } else {
-      const int idx = item_at(round, p.n_items);
-      if (idx < 0) break;
-      decode_item(p, idx, b, h, qb);
+      const int u = item_at(round, p.n_units);
+      if (u < 0) break;
+      decode_unit<SPLIT>(p, u, w);
       if constexpr (C::kFp8) {
-        const int di = p.descale_per_bkv ? b * p.Hkv + h / p.group : 0;
+        const int di = p.descale_per_bkv ? w.b * p.Hkv + w.h / p.group : 0;
         dqk = __ldg(p.dq + di) * __ldg(p.dk + di);
         dvv = __ldg(p.dv + di);
       }
     }
-    const int nk = kv_tiles_for(p, qb, t);
+    const int b = w.b, h = w.h, qb = w.qb;
+    const int j0 = SPLIT ? w.j0 : 0;
+    const int nk = SPLIT ? (t ? w.end1 : w.end0) : kv_tiles_for(p, qb, t);
     const float lam = log2e * p.scale * dqk;  // log2 units per unit of s
     const float lam8 = 8.0f * lam;            // Lean-P code units per unit of s
     const float lamc = lam8 * (1.0f / 128.0f);
@@ -652,11 +746,11 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
     float ref = 0.0f;  // Lean-P: reference binade; exact paths: running max (log2 units)
     bool have_ref = false;
     const bool stamp = round == 0 && r == 0;
-    for (int j = 0; j < nk; ++j) {
+    for (int j = j0; j < nk; ++j) {
       if (stamp) FA8_TL(t, j, 0);
       if (!warp_wait(&bars.s_full[t], s_cnt & 1, ab, lim)) return;
       if (stamp) FA8_TL(t, j, 1);
-      if (j == 0 && r == 0) FA8_TL(5, round, 4 * t);
+      if (j == j0 && r == 0) FA8_TL(5, round, 4 * t);
       ++s_cnt;
       tc_fence_after();
       uint32_t s[128];
@@ -803,7 +897,7 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
       // P_t(j-1) must have been consumed, and O_t must be final for j-1
       // before it is corrected for a raised reference.
       auto wait_o_and_rescale = [&]() -> bool {
-        if (j > 0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return false;
+        if (j > j0 && !warp_wait(&bars.o_done[t], (o_cnt - 1) & 1, ab, lim)) return false;
         if constexpr (V == kLeanPA3) {
           // frequent, non-power-of-two: 32-column passes with packed multiplies
           // (the second block's scores are still live here) and the row-sum column
@@ -900,6 +994,139 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
       mbar_arrive(&bars.o_free[t]);
       if (r == 0) FA8_TL(5, round, 4 * t + 2);
       if constexpr (C::kBlockScaled) l = __uint_as_float(lsum);
+      if constexpr (SPLIT) {
+        // the piece is worked out again from the unit index here, so that
+        // the key-tile loop carries one register for it instead of three
+        const int ns = p.split_ns, sidx = w.u / ns, piece = w.u - sidx * ns;
+        if (w.u < p.n_split_items * ns) {
+          // One piece of a split item: O, l and ref (O and l relative to
+          // 2^ref) go to the workspace; the piece that arrives last adds the
+          // pieces up in piece order (exact power-of-two rescales to the
+          // largest ref), so the sum does not depend on which piece it is,
+          // and writes the output.  The others are done with this unit.
+          float* slots = reinterpret_cast<float*>(p.ws + split_cnt_bytes(p.n_split_items));
+          auto slot = [&](int s) {
+            return slots + ((size_t)(sidx * ns + s) * 2 + t) * kSplitSlotFloats;
+          };
+          float* mine = slot(piece);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            __stcg(reinterpret_cast<float4*>(mine) + c * 128 + r,
+                   make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
+                               __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3])));
+          __stcg(mine + 128 * 128 + r, l);
+          __stcg(mine + 128 * 129 + r, ref2);
+          __threadfence();
+          // the tile's four warps: every row's partial is written and fenced
+          // (an mbarrier, so that the wait is bounded like every other)
+          auto group_sync = [&]() {
+            mbar_arrive(&bars.split_sync[t]);
+            return warp_wait(&bars.split_sync[t], (sync_cnt++) & 1, ab, lim);
+          };
+          if (!group_sync()) return;
+          if (r == 0) bars.split_last[t] = split_arrive(p, sidx, ns, t, ab) ? 1 : 0;
+          if (!group_sync()) return;
+          if (!bars.split_last[t]) continue;
+          __threadfence();
+          // every piece from the workspace (this one's too), in piece order,
+          // rescaled to the largest reference: the output straight from the
+          // sums, four columns at a time (no 128-value array in registers)
+          float R = -INFINITY;
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            if (s < ns) R = fmaxf(R, __ldcg(slot(s) + 128 * 129 + r));
+          float sc[4];
+          float L = 0.0f;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            sc[s] = 0.0f;
+            if (s < ns) {
+              const float d = __ldcg(slot(s) + 128 * 129 + r) - R;  // integers: exact, <= 0
+              sc[s] = d < -126.0f ? 0.0f : pow2i((int)d);
+              L = fmaf(__ldcg(slot(s) + 128 * 128 + r), sc[s], L);
+            }
+          }
+          const float inv = dvv / L;
+          if (p.lse && store)
+            p.lse[((size_t)b * p.Hq + h) * p.S + row] = (R + log2f(L)) * 0.6931471805599453f;
+          // 32 output columns at a time: every piece's values are loaded
+          // before any of the group's stores, so the loads of a group are in
+          // flight together instead of waiting behind stores that might alias
+          auto sum32 = [&](int g, float (&y)[32]) {  // columns 32g .. 32g+31
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = 0.0f;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+              if (s < ns) {
+                float4 x[8];
+                const float4* src = reinterpret_cast<const float4*>(slot(s)) + (8 * g) * 128 + r;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + i * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  y[4 * i] = fmaf(x[i].x, sc[s], y[4 * i]);
+                  y[4 * i + 1] = fmaf(x[i].y, sc[s], y[4 * i + 1]);
+                  y[4 * i + 2] = fmaf(x[i].z, sc[s], y[4 * i + 2]);
+                  y[4 * i + 3] = fmaf(x[i].w, sc[s], y[4 * i + 3]);
+                }
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] *= inv;
+          };
+          auto bf16x8 = [&](const float (&y)[32], int c) {  // y[8c .. 8c+7] as eight bf16
+            uint32_t w4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 hv = __floats2bfloat162_rn(y[8 * c + 2 * k], y[8 * c + 2 * k + 1]);
+              w4[k] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            return make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          };
+          if (C::kEpiTma && !p.out_f32) {
+            // as the whole-item epilogue below: this warp's slot, TMA stores
+            uint8_t* oslot = smem + C::kSmemOut + (t * 4 + quad) * C::kOutSlotBytes;
+            const int row0 = qb * 256 + t * 128 + (int)quad * 32;
+            const uint32_t lane = lane_id();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+              float y0[32], y1[32];
+              sum32(2 * half, y0);
+              sum32(2 * half + 1, y1);
+              if (lane == 0) bulk_wait_read_all();
+              __syncwarp();
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                *reinterpret_cast<uint4*>(oslot + lane * 128 + ((c ^ (lane & 7)) * 16)) = bf16x8(y0, c);
+                *reinterpret_cast<uint4*>(oslot + lane * 128 + (((c + 4) ^ (lane & 7)) * 16)) =
+                    bf16x8(y1, c);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 < p.S) {
+                tma_store_4d(&maps.o64, oslot, 64 * half, h, row0, b);
+                bulk_commit();
+              }
+            }
+          } else if (store) {
+#pragma unroll 1
+            for (int g = 0; g < 4; ++g) {
+              float y[32];
+              sum32(g, y);
+              if (p.out_f32) {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV) + 8 * g;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV) + 4 * g;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) dst[c] = bf16x8(y, c);
+              }
+            }
+          }
+          continue;
+        }
+      }
       const float inv = dvv / l;
       if (p.lse && store)
         p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
@@ -1000,10 +1227,12 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
 // --------------------------------------------------------------------------
 // The kernel.
 // --------------------------------------------------------------------------
-template <int V, int DQK>
+template <int V, int DQK, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ Maps maps, const KParams p) {
   using C = Cfg<V, DQK>;
+  // the split schedule needs codes that depend on each 64-key block alone
+  static_assert(!SPLIT || V == kLeanP || V == kBlockExact, "split units: block-local codes only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1030,6 +1259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) mbar_init(&bars.qk_go[t][i], 1);
       mbar_init(&bars.o_free[t], 128);
       mbar_init(&bars.drain[t], 1);
+      mbar_init(&bars.split_sync[t], 128);
     }
     fence_mbar_init();
   }
@@ -1062,18 +1292,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp < 8) {
-    softmax_loop<V, DQK>(p, maps, smem, bars, tmem, warp / 4);
+    softmax_loop<V, DQK, SPLIT>(p, maps, smem, bars, tmem, warp / 4);
     // bulk stores of the output must be complete before the CTA exits
     if (C::kEpiTma && lane_id() == 0) bulk_wait_all();
     __syncwarp();
   } else if (warp == kProducerWarp) {
-    producer_loop<V, DQK>(p, maps, smem, bars);
+    producer_loop<V, DQK, SPLIT>(p, maps, smem, bars);
   } else if (warp == kQkWarp || warp == kPvWarp) {
     const int role = warp == kQkWarp ? 0 : 1;
     if (role == 0)
-      qk_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
+      qk_loop<V, DQK, SPLIT>(p, smem_u32(smem), bars, tmem);
     else
-      pv_loop<V, DQK>(p, smem_u32(smem), bars, tmem);
+      pv_loop<V, DQK, SPLIT>(p, smem_u32(smem), bars, tmem);
     if (lane_id() == 0) {
       // every MMA this thread issued must be complete before TMEM is released;
       // a drain that runs out of time is reported like any other expired wait

@@ -58,9 +58,11 @@
  * (128, 128) for BF16, any S >= 1, B >= 1, Hq % Hkv == 0.  Base addresses must
  * be 16-byte aligned.  The device must be sm_103 (GB300).
  *
- * Ownership and threading: the caller owns every buffer.  The library keeps
- * no per-call allocations and no global mutable state besides a per-device
- * cache of kernel attributes; calls on different streams may run concurrently.
+ * Ownership and threading: the caller owns every buffer, including the
+ * optional workspace of attn_fwd_full.  The library allocates no device
+ * memory and keeps no global mutable state besides a per-device cache of
+ * kernel attributes, a cache of split schedules and a call counter; calls on
+ * different streams may run concurrently (each with its own workspace).
  * Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
  * stream); argument errors are returned synchronously before anything is
  * launched.
@@ -68,11 +70,13 @@
 #ifndef FP8ATTN_H
 #define FP8ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 7
+#define FP8ATTN_API_VERSION 8
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -196,13 +200,41 @@ int attn_launches_per_call(void);
  *              unnormalised weights (Lean-P: the rounded, scaled weights whose
  *              sum divides the output; exact paths: exp(z_ij) before rounding),
  *              z_ij = softmax_scale * descale_q * descale_k * <q_i, k_j>
+ *   workspace, workspace_bytes
+ *              NULL (and 0), or device memory of at least the size that
+ *              attn_workspace_size reports for the same arguments, 256-byte
+ *              aligned, owned by the caller and used by one call at a time
+ *              (calls that overlap on the GPU need workspaces of their own).
+ *              With it, problems with too few work items to fill every SM
+ *              (few heads, short sequences) split their longest items along
+ *              the keys into pieces that run on different SMs and are added up
+ *              by the piece that finishes last (ATTN_VARIANT_LEANP and
+ *              ATTN_VARIANT_BLOCK_EXACT, whose codes depend on each 64-key
+ *              block alone, so a split changes only the order of the fp32
+ *              sums; the pieces are added in a fixed order, so the result is
+ *              the same on every call).  The memory needs no clearing: it holds
+ *              partial results and counters tagged with a per-call number.
+ *              Too small a workspace is an ATTN_ERR_INVALID_ARG; NULL runs
+ *              every item whole, as attn_fwd_ex does.
  * Other arguments as attn_fwd_ex.  Returns an attn_status.
  */
 int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
                   const float* descale_q, const float* descale_k, const float* descale_v,
                   void* out, int out_dtype, float* lse, int B, int Hq, int Hkv, int S, int Dqk,
                   int Dv, int causal, float softmax_scale, int flags, int* dev_status,
-                  void* stream);
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace attn_fwd_full uses for these arguments on the CURRENT
+ * device (its SM count enters the schedule): 0 when the problem runs without
+ * splitting (enough work items, another variant, or
+ * ATTN_FLAG_TEST_CHUNK_UNITS), otherwise at most 128 MiB.  The split
+ * schedule is chosen by a model of the kernel's time per key tile and per
+ * work unit; it is cached per shape.  Returns an attn_status; *bytes is 0 on
+ * error.
+ */
+int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                        int flags, size_t* bytes);
 
 /* Input element type for attn_quantize_fp8. */
 typedef enum { ATTN_IN_BF16 = 0, ATTN_IN_F32 = 1 } attn_in_dtype;

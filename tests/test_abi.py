@@ -18,14 +18,15 @@ def test_header_declares_the_entry_points():
     names = fa.declared_functions()
     for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
               "attn_quantize_fp8", "attn_fwd_full", "attn_status_string",
-              "attn_launches_per_call", "attn_api_version", "attn_debug_timeline"):
+              "attn_launches_per_call", "attn_api_version", "attn_debug_timeline",
+              "attn_workspace_size"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 7
+    assert lib.attn_api_version() == 8
     assert lib.attn_launches_per_call() == 1
 
 
@@ -109,11 +110,33 @@ def test_full_entry_point_checks_arguments(lib):
     f = lib.attn_fwd_full
     args = lambda **kw: [kw.get("variant", 0), P, P, P, P, P, P, P, 0, kw.get("lse", None), 1, 2, 2,
                          128, 128, kw.get("Dv", 128), kw.get("causal", 1), 0.0, kw.get("flags", 0),
-                         None, None]
+                         None, kw.get("ws", None), kw.get("ws_bytes", 0), None]
     assert f(*args(lse=MIS)) == fa.ATTN_ERR_INVALID_ARG                  # misaligned lse
     assert f(*args(flags=8)) == fa.ATTN_ERR_INVALID_ARG                  # unknown flag
     assert f(*args(causal=-1)) == fa.ATTN_ERR_INVALID_ARG
     assert f(*args(Dv=64, flags=fa.ATTN_FLAG_DESCALE_PER_BKV)) == fa.ATTN_ERR_UNSUPPORTED
+    # the workspace must be 256-byte aligned (checked before the device)
+    assert f(*args(ws=ctypes.c_void_p(0x10010), ws_bytes=1 << 20)) == fa.ATTN_ERR_INVALID_ARG
+
+
+def test_workspace_size_query(lib):
+    """attn_workspace_size: argument errors, and 0 (no split, no device
+    needed) for the variants whose codes depend on the running maximum and
+    for problems whose K and V are large enough for the chunked order."""
+    n = ctypes.c_size_t(123)
+    q = lambda *a, **kw: lib.attn_workspace_size(*a, ctypes.byref(n))
+    assert lib.attn_workspace_size(0, 1, 2, 2, 128, 128, 128, 1, 0, None) == fa.ATTN_ERR_INVALID_ARG
+    assert q(0, 1, 3, 2, 128, 128, 128, 1, 0) == fa.ATTN_ERR_INVALID_ARG and n.value == 0  # Hq % Hkv
+    assert q(9, 1, 2, 2, 128, 128, 128, 1, 0) == fa.ATTN_ERR_INVALID_ARG                 # variant
+    assert q(0, 1, 2, 2, 128, 128, 128, 2, 0) == fa.ATTN_ERR_INVALID_ARG                 # causal
+    for variant in (fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_BF16, fa.ATTN_VARIANT_LEANP_A3):
+        n.value = 123
+        assert q(variant, 1, 8, 8, 4096, 128, 128, 1, 0) == fa.ATTN_OK and n.value == 0
+    n.value = 123
+    assert q(0, 1, 8, 8, 4096, 128, 128, 1, fa.ATTN_FLAG_TEST_CHUNK_UNITS) == fa.ATTN_OK
+    assert n.value == 0
+    n.value = 123
+    assert q(0, 1, 32, 32, 65536, 128, 128, 1, 0) == fa.ATTN_OK and n.value == 0      # chunked
 
 
 def test_release_library_has_no_timeline(lib):

@@ -285,7 +285,7 @@ def test_no_write_outside_output_and_lse(variant, S, causal, out_dtype):
         ptrs = ptrs + [None, None, None]
     st = lib.attn_fwd_full(int(variant), *ptrs, ctypes.c_void_p(out.data_ptr()), int(out_dtype),
                            ctypes.c_void_p(lse_view.data_ptr()), B, Hq, Hkv, S, 128, 128,
-                           int(causal), ctypes.c_float(0.0), 0, None,
+                           int(causal), ctypes.c_float(0.0), 0, None, None, 0,
                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == fa.ATTN_OK, fa.status_string(st)
     torch.cuda.synchronize()
@@ -321,9 +321,9 @@ def test_chunked_item_order_gives_the_same_bits(variant, causal):
         q, k, v, d = dev_fp8(wl.fp8_gaussian_case(2, 12, 3, 2100, 128, 128, seeds=(73, 74, 75)))
         args = (q, k, v, *d)
     plain = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
-                             return_lse=True)
+                             return_lse=True, split=False)
     chunked = fa.attn_fwd_full(variant, *args, out_dtype=fa.ATTN_OUT_F32, causal=causal,
-                               return_lse=True, flags=fa.ATTN_FLAG_TEST_CHUNK_UNITS)
+                               return_lse=True, flags=fa.ATTN_FLAG_TEST_CHUNK_UNITS, split=False)
     torch.cuda.synchronize()
     assert torch.equal(plain[0], chunked[0]) and torch.equal(plain[1], chunked[1])
 

@@ -1,0 +1,182 @@
+"""GPU parity of the split schedule (attn_fwd_full with a workspace).
+
+Problems with too few work items to keep every SM busy (few heads, short
+sequences) split their longest items along the keys into pieces that run on
+different SMs; the piece that finishes last adds the pieces' partial results
+(O and the rounded row sum, relative to each piece's power-of-two reference)
+and writes the output.  Lean-P's codes and block scales depend on each 64-key
+block alone ("Zyphra ZYFA: FP8 FlashAttention for AMD MI355X", "Lean P: one
+multiply-add instead of an exponential" and "Per-block scaling and a rounded
+row sum"), so a split changes only the order of the fp32 sums.
+
+Checks, on shapes the schedule splits (asserted through workspace_size):
+- sampled rows against the oracle's emulation of the same path, with the
+  usual per-row gate, and the log-sum-exp;
+- the whole output and LSE against the same call without splitting, within
+  fp32 reassociation;
+- the same bits on every call, with fresh workspaces and with a workspace
+  filled with garbage (its counters need no clearing), and for two problems
+  that alternate on one workspace;
+- bf16 output equal to the fp32 output rounded, and no write outside the
+  output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_causal_prefill_flash_gb300 as fa
+import oracle
+from fp8_causal_prefill_flash_gb300 import workloads as wl
+
+from gpu_helpers import check_rows
+
+pytestmark = pytest.mark.gpu
+
+PATH = {fa.ATTN_VARIANT_LEANP: "leanp", fa.ATTN_VARIANT_BLOCK_EXACT: "variant_e"}
+
+# (B, Hq, Hkv, S, Dqk, causal, per-(batch, kv head) descales)
+SHAPES = {
+    "h8_s2048": (1, 8, 8, 2048, 128, True, False),
+    "gqa_b2_ragged": (2, 8, 2, 1500, 128, True, False),
+    "noncausal_h4": (1, 4, 4, 2000, 128, False, False),
+    "mla_h4": (1, 4, 4, 2048, 192, True, False),
+    "h2_s4096": (1, 2, 2, 4096, 128, True, False),
+    "per_bkv_b2": (2, 4, 2, 2048, 128, True, True),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fa.build()
+    fa.load_library()
+
+
+def make(name, seed):
+    B, Hq, Hkv, S, Dqk, causal, per_bkv = SHAPES[name]
+    case = wl.fp8_gaussian_case(B, Hq, Hkv, S, Dqk, 128, seeds=(seed, seed + 1, seed + 2))
+    if per_bkv:
+        rng = np.random.default_rng(seed + 3)
+        dq, dk, dv = (case.dq * rng.uniform(0.5, 2.0, (B, Hkv)) for _ in range(3))
+    else:
+        dq, dk, dv = case.dq, case.dk, case.dv
+    q, k, v = (torch.from_numpy(a).cuda() for a in (case.q, case.k, case.v))
+    d = [torch.from_numpy(np.asarray(x, np.float32).reshape(-1).copy()).cuda() for x in (dq, dk, dv)]
+    return case, (q, k, v, *d), (dq, dk, dv), causal
+
+
+def call(variant, args, causal, split=True, out_dtype=fa.ATTN_OUT_F32, workspace=None,
+         status=None):
+    out, lse = fa.attn_fwd_full(variant, *args, out_dtype=out_dtype, causal=causal,
+                                return_lse=True, split=split, workspace=workspace,
+                                dev_status=status)
+    return out, lse
+
+
+def sample_rows(B, Hq, S, seed, n=700):
+    rng = np.random.default_rng(seed)
+    edge = [0, 1, 127, 128, 255, 256, S // 2, S - 2, S - 1]
+    rows = [(b, h, i) for b in range(B) for h in range(min(Hq, 2)) for i in edge if 0 <= i < S]
+    rows += list(zip(rng.integers(0, B, n), rng.integers(0, Hq, n), rng.integers(0, S, n)))
+    return np.asarray(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_BLOCK_EXACT])
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_split_matches_the_oracle_and_the_whole_items(name, variant):
+    case, args, (dq, dk, dv), causal = make(name, 500)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    need = fa.workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal)
+    assert need > 0, "the schedule should split this problem"
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = call(variant, args, causal, status=status)
+    plain, plain_lse = call(variant, args, causal, split=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.ATTN_OK, fa.status_string(int(status.item()))
+
+    # the whole output: only the order of the fp32 sums differs
+    scale = float(plain.abs().max())
+    assert float((out - plain).abs().max()) <= 2e-6 * scale + 1e-30
+    assert float((lse - plain_lse).abs().max()) <= 2e-6 * (1.0 + float(plain_lse.abs().max()))
+
+    # sampled rows against the emulation of the same path
+    rows = sample_rows(B, Hq, S, 501)
+    want, amb, want_lse = oracle.attention(PATH[variant], case.q, case.k, case.v, dq, dk, dv,
+                                           rows=rows, causal=causal)
+    gpu = out.cpu().numpy().astype(np.float64)
+    got = np.stack([gpu[b, i, h] for b, h, i in rows])
+    vmax = float(np.max(np.abs(oracle.e4m3_decode(case.v)))) * float(np.max(dv))
+    check_rows(got, want, amb, vmax)
+    glse = lse.cpu().numpy().astype(np.float64)
+    got_lse = np.array([glse[b, h, i] for b, h, i in rows])
+    a = np.minimum(amb, 0.5)
+    assert np.all(np.abs(got_lse - want_lse) <= 2e-5 * (1 + np.abs(want_lse)) + 2.0 * a / (1.0 - a))
+
+
+@pytest.mark.parametrize("name", ["h8_s2048", "gqa_b2_ragged", "mla_h4"])
+def test_split_is_deterministic_with_any_workspace(name):
+    variant = fa.ATTN_VARIANT_LEANP
+    case, args, _, causal = make(name, 520)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    need = fa.workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal)
+    assert need > 0
+    first = call(variant, args, causal)
+    outs = [call(variant, args, causal) for _ in range(3)]  # fresh workspaces
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs.append(call(variant, args, causal, workspace=ws))
+    ws.random_(0, 256)
+    outs.append(call(variant, args, causal, workspace=ws))
+    outs.append(call(variant, args, causal, workspace=ws))  # counters left by the call before
+    torch.cuda.synchronize()
+    for o, l in outs:
+        assert torch.equal(o, first[0]) and torch.equal(l, first[1])
+
+
+def test_two_problems_alternate_on_one_workspace():
+    variant = fa.ATTN_VARIANT_LEANP
+    case_a, args_a, _, causal_a = make("h8_s2048", 540)
+    case_b, args_b, _, causal_b = make("h2_s4096", 550)
+    need = max(fa.workspace_size(variant, *c.shape, causal) for c, causal in
+               ((case_a, causal_a), (case_b, causal_b)))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    want_a = call(variant, args_a, causal_a)
+    want_b = call(variant, args_b, causal_b)
+    got = []
+    for _ in range(3):
+        got.append(call(variant, args_a, causal_a, workspace=ws))
+        got.append(call(variant, args_b, causal_b, workspace=ws))
+    torch.cuda.synchronize()
+    for i, (o, l) in enumerate(got):
+        want = want_a if i % 2 == 0 else want_b
+        assert torch.equal(o, want[0]) and torch.equal(l, want[1]), i
+
+
+@pytest.mark.parametrize("name", ["h8_s2048", "gqa_b2_ragged", "noncausal_h4"])
+def test_split_bf16_output_is_the_fp32_output_rounded(name):
+    """The last piece writes bf16 through the same shared-memory slot and
+    TMA stores as a whole item; the values are the fp32 output rounded."""
+    variant = fa.ATTN_VARIANT_LEANP
+    case, args, _, causal = make(name, 560)
+    f32, _ = call(variant, args, causal)
+    b16, _ = call(variant, args, causal, out_dtype=fa.ATTN_OUT_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(b16, f32.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("out_dtype", [fa.ATTN_OUT_F32, fa.ATTN_OUT_BF16])
+def test_split_writes_every_output_element_and_nothing_else(out_dtype):
+    variant = fa.ATTN_VARIANT_LEANP
+    case, args, _, causal = make("gqa_b2_ragged", 580)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    esz = 4 if out_dtype == fa.ATTN_OUT_F32 else 2
+    n_out = B * S * Hq * Dv * esz
+    pad = 4096
+    raw = torch.full((pad + n_out + pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    dt = torch.float32 if out_dtype == fa.ATTN_OUT_F32 else torch.bfloat16
+    out = raw[pad:pad + n_out].view(dt).view(B, S, Hq, Dv)
+    fa.attn_fwd_full(variant, *args, out=out, out_dtype=out_dtype, causal=causal)
+    torch.cuda.synchronize()
+    h = raw.cpu().numpy()
+    assert np.all(h[:pad] == 0xA5) and np.all(h[-pad:] == 0xA5)
+    words = h[pad:pad + n_out].view(np.uint32 if esz == 4 else np.uint16)
+    assert not np.any(words == (0xA5A5A5A5 if esz == 4 else 0xA5A5))
