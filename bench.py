@@ -639,7 +639,51 @@ def extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms, n):
                      "clocks": clk}
         del q, k, v, o
         torch.cuda.empty_cache()
+    legs["leanp_few_heads_split"] = split_leg(torch, fa, wl, dev, peaks, n)
     return legs
+
+
+def split_leg(torch, fa, wl, dev, peaks, n):
+    """Lean-P on few heads (fp8_h4_s8k_d128: 128 work items for the SMs),
+    with the split schedule (attn_fwd_full and a workspace) and with whole
+    items.  The inputs fit in L2, so a 256 MB buffer is written before every
+    timed call and only the call is timed."""
+    name = "fp8_h4_s8k_d128"
+    case = wl.make_case(name)
+    B, Hq, Hkv, S, Dqk, Dv = case.shape
+    F = causal_flops(B, Hq, S, Dqk, Dv)
+    q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+    d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+    o = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
+    need = fa.workspace_size(fa.ATTN_VARIANT_LEANP, B, Hq, Hkv, S, Dqk, Dv, True)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {"workload": name, "unit": "TFLOP/s", "workspace_bytes": need, "steps": n,
+           "l2": "256 MB written before every timed call"}
+    for key, split in (("split", True), ("whole", False)):
+        def fn():
+            fa.attn_fwd_full(fa.ATTN_VARIANT_LEANP, q, k, v, *d, out=o, split=split,
+                             workspace=ws if need else None)
+        for _ in range(5):
+            fn()
+        total = 0.0
+        for _ in range(n):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        ms = total / n
+        out[key] = {"value": F / (ms * 1e-3) / 1e12, "ms_per_step": ms}
+    peak = peaks["bf16_burst"] * FP8_OVER_BF16
+    out["value"] = out["split"]["value"]
+    out["frac"] = out["value"] / peak
+    out["speedup_over_whole_items"] = out["split"]["value"] / out["whole"]["value"]
+    del q, k, v, o, ws, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 # --only PATH: the workload each path is profiled on (headline FP8 shape, the
@@ -814,6 +858,9 @@ def run_sweep(args):
             q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
             d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
             paths = {"leanp": lambda: fa.attn_fwd_fp8(q, k, v, *d, out=out),
+                     # with the split schedule where the problem has few work items
+                     "leanp_split": lambda: fa.attn_fwd_full(fa.ATTN_VARIANT_LEANP, q, k, v, *d,
+                                                             out=out),
                      "exact_fp8_ablation": lambda: fa.attn_fwd_fp8_exact(q, k, v, *d, out=out),
                      # Lean-P's block scale and rounded sum, exponential for the code
                      "block_exact": lambda: fa.attn_fwd_ex(fa.ATTN_VARIANT_BLOCK_EXACT, q, k, v,
