@@ -525,3 +525,59 @@ int attn_debug_timeline(unsigned long long* host, int capacity, int reset) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ no-alloc entry
+// attn_fwd_fp8_noalloc: attn_fwd_fp8 with the split schedule of attn_fwd_full
+// for callers that cannot allocate device memory.  Some code may not call
+// cudaMalloc: a plugin or runtime that owns every device allocation through
+// its own allocator, a real-time or inference loop that forbids allocations
+// after start-up (an allocation can synchronise the device and stall other
+// streams), or code that runs with a fixed memory budget.  Such callers can
+// still pass inputs and outputs, but not a workspace, so the split schedule
+// takes its scratch from this array: file-scope device memory that the driver
+// sets aside when the library's module loads, on every GPU that loads it, and
+// keeps until the process exits.  The split schedule tags its counters with a
+// per-call number, so nothing in the array has to start at zero and nothing
+// is cleared between calls; every call shares the array, so calls that
+// overlap on the GPU (different streams) race on it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// The device address of g_noalloc_scratch on the current device.  In host
+// code the array's name stands for a host-side shadow, not device memory, so
+// the address comes from cudaGetSymbolAddress, once per device, with that
+// device current.
+int noalloc_scratch(void** ptr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return ATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_fp8_noalloc(const void* q, const void* k, const void* v,
+                                    const float* descale_q, const float* descale_k,
+                                    const float* descale_v, void* out, int B, int Hq, int Hkv,
+                                    int S, int Dqk, int Dv, int causal, void* stream) {
+  // the schedule attn_fwd_full would choose with a workspace, and its scratch
+  size_t need = 0;
+  int st = attn_workspace_size(ATTN_VARIANT_LEANP, B, Hq, Hkv, S, Dqk, Dv, causal, 0, &need);
+  if (st != ATTN_OK) return st;
+  if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
+  return run(ATTN_VARIANT_LEANP, q, k, v, descale_q, descale_k, descale_v, out, ATTN_OUT_BF16,
+             nullptr, B, Hq, Hkv, S, Dqk, Dv, causal, 0.0f, 0, nullptr, need ? scratch : nullptr,
+             need ? (size_t)ATTN_NOALLOC_SCRATCH_BYTES : 0, stream);
+}

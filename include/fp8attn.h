@@ -266,6 +266,38 @@ typedef enum { ATTN_IN_BF16 = 0, ATTN_IN_F32 = 1 } attn_in_dtype;
 int attn_quantize_fp8(const void* x, int in_dtype, void* codes, float* descale, int B, int S,
                       int H, int D, int hadamard, void* stream);
 
+/* Bytes of device scratch that attn_fwd_fp8_noalloc holds (32 MiB). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * attn_fwd_fp8 for callers that cannot allocate device memory, with the split
+ * schedule of attn_fwd_full.  (The articles have no counterpart: this is an
+ * interface for callers of this library.)  Some callers may not call
+ * cudaMalloc: a framework or runtime that owns every device allocation
+ * through its own allocator, a serving loop that allows no allocation after
+ * start-up (an allocation can synchronise the device and stall the other
+ * streams), or code with a fixed memory budget.  They pass inputs and
+ * outputs as for attn_fwd_fp8 (same arguments, same result as attn_fwd_full
+ * with a workspace), and the scratch that the split schedule needs comes from
+ * a file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array, which keeps the last call's contents;
+ *     nothing in it needs clearing (the schedule tags its counters per call).
+ *     Calls that overlap on the GPU (on different streams) race on the array
+ *     and give wrong results: order them on one stream.
+ *   - A problem whose split schedule needs more than ATTN_NOALLOC_SCRATCH_BYTES
+ *     (attn_workspace_size reports the size) is rejected with
+ *     ATTN_ERR_UNSUPPORTED before anything is launched.
+ * Returns an attn_status.
+ */
+int attn_fwd_fp8_noalloc(const void* q, const void* k, const void* v, const float* descale_q,
+                         const float* descale_k, const float* descale_v, void* out, int B, int Hq,
+                         int Hkv, int S, int Dqk, int Dv, int causal, void* stream);
+
 /* Library ABI version (FP8ATTN_API_VERSION of the build). */
 int attn_api_version(void);
 
