@@ -417,20 +417,24 @@ def run_ours(args, rank, world, local_rank):
     def step():
         fa.attn_fwd_fp8(q, k, v, *d, out=out)
 
-    def timed(fn, n, warm):
+    per_launch = []
+
+    def timed(fn, n, warm, record=False):
         for _ in range(warm):
             fn()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        evs[0].record(stream)
+        for i in range(n):
             fn()
-        e1.record(stream)
+            evs[i + 1].record(stream)  # per-launch times: an event between launches
         torch.cuda.synchronize()
         barrier()
-        return max_over_ranks(e0.elapsed_time(e1) / n, dev)
+        if record:
+            per_launch[:] = [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+        return max_over_ranks(evs[0].elapsed_time(evs[n]) / n, dev)
 
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -445,7 +449,7 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     e_start = meter.read_mj()
-    ms = timed(step, args.steps, 0)
+    ms = timed(step, args.steps, 0, record=True)
     e_end = meter.read_mj()
     clk = clocks.stop()
     h_timed = output_sha256(out)
@@ -508,6 +512,9 @@ def run_ours(args, rank, world, local_rank):
     per_gpu = F / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": job_tflops(F, world, ms), "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "ms_per_launch": {"median": statistics.median(per_launch), "min": min(per_launch),
+                              "max": max(per_launch),
+                              "how": "CUDA events between the timed launches (this rank)"},
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": job_tflops(F, world, ms) / PAGES_TFLOPS, "vs_baseline_note": PAGES_NOTE,
             "dtype": "fp8_e4m3 (fp32 accumulate)", "data": "synthetic",
