@@ -1133,7 +1133,9 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
       if (C::kEpiTma && !p.out_f32) {
         // bf16 rows through this warp's shared-memory slot and TMA stores (the
         // tensor map clips rows past S): the warp does not wait for global
-        // memory, only for the slot's previous contents to have been read
+        // memory, only for the slot's previous contents to have been read.
+        // The normalisation runs on packed pairs (measured 0.2-2.5% faster
+        // than scalar multiplies, most at short sequences).
         uint8_t* slot = smem + C::kSmemOut + (t * 4 + quad) * C::kOutSlotBytes;
         const int row0 = qb * 256 + t * 128 + (int)quad * 32;
         const uint32_t lane = lane_id();
@@ -1147,8 +1149,10 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int col = 64 * half + 8 * c + 2 * k;
-              __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(o[col]) * inv,
-                                                        __uint_as_float(o[col + 1]) * inv);
+              uint32_t x0, x1;
+              f32x2_unpack(mul_f32x2(f32x2_pack(__uint_as_float(o[col]), __uint_as_float(o[col + 1])),
+                                     f32x2_pack(inv, inv)), x0, x1);
+              __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(x0), __uint_as_float(x1));
               w[k] = *reinterpret_cast<uint32_t*>(&hv);
             }
             *reinterpret_cast<uint4*>(slot + lane * 128 + ((c ^ (lane & 7)) * 16)) =
