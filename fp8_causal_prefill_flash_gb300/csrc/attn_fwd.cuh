@@ -318,7 +318,10 @@ __device__ __forceinline__ void decode_unit(const KParams& p, int u, Unit& w) {
 // its partial result is in the workspace (and fenced): true for the piece
 // that arrives last.  The counter holds (epoch << 3) + pieces arrived; a
 // value with another epoch (an earlier call, or memory never used) counts as
-// zero, so the workspace needs no clearing between calls.
+// zero, so the workspace needs no clearing between calls.  The last piece
+// sets the counter back to zero: every piece of this call has arrived, and a
+// replay of the same launch from a CUDA graph, which repeats its epoch, then
+// starts from zero too.
 __device__ __forceinline__ bool split_arrive(const KParams& p, int sidx, int ns, int t,
                                              volatile int* ab) {
   unsigned long long* cnt = reinterpret_cast<unsigned long long*>(p.ws) + (size_t)sidx * 2 + t;
@@ -334,7 +337,9 @@ __device__ __forceinline__ bool split_arrive(const KParams& p, int sidx, int ns,
     }
   }
   const unsigned long long before = (old >> 3) == p.epoch ? (old & 7ull) : 0ull;
-  return before == (unsigned long long)(ns - 1);
+  const bool last = before == (unsigned long long)(ns - 1);
+  if (last) atomicExch(cnt, 0ull);
+  return last;
 }
 
 struct __align__(8) Barriers {

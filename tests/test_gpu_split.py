@@ -180,3 +180,32 @@ def test_split_writes_every_output_element_and_nothing_else(out_dtype):
     assert np.all(h[:pad] == 0xA5) and np.all(h[-pad:] == 0xA5)
     words = h[pad:pad + n_out].view(np.uint32 if esz == 4 else np.uint16)
     assert not np.any(words == (0xA5A5A5A5 if esz == 4 else 0xA5A5))
+
+
+def test_split_call_replays_from_a_cuda_graph():
+    """A captured call replays with the same parameters, its per-call tag
+    included; the last piece resets the counters, so every replay combines
+    its own pieces.  New inputs are copied in between replays."""
+    variant = fa.ATTN_VARIANT_LEANP
+    case_a, args_a, _, causal = make("h8_s2048", 590)
+    case_b, args_b, _, _ = make("h8_s2048", 595)
+    q, k, v, dq, dk, dv = (t.clone() for t in args_a)
+    out = torch.empty((1, 2048, 8, 128), dtype=torch.bfloat16, device="cuda")
+    need = fa.workspace_size(variant, 1, 8, 8, 2048, 128, 128, causal)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    run = lambda: fa.attn_fwd_full(variant, q, k, v, dq, dk, dv, out=out, causal=causal,
+                                   workspace=ws)
+    run()  # eager warm-up: library loaded, plan cached
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for src in (args_b, args_a, args_b):
+        for dst, x in zip((q, k, v, dq, dk, dv), src):
+            dst.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        want = fa.attn_fwd_full(variant, *src, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
