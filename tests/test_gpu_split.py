@@ -42,6 +42,7 @@ SHAPES = {
     "mla_h4": (1, 4, 4, 2048, 192, True, False),
     "h2_s4096": (1, 2, 2, 4096, 128, True, False),
     "per_bkv_b2": (2, 4, 2, 2048, 128, True, True),
+    "h1_s32k": (1, 1, 1, 32768, 128, True, False),  # pieces of about 128 key tiles
 }
 
 
