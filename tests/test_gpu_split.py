@@ -43,6 +43,7 @@ SHAPES = {
     "h2_s4096": (1, 2, 2, 4096, 128, True, False),
     "per_bkv_b2": (2, 4, 2, 2048, 128, True, True),
     "h1_s32k": (1, 1, 1, 32768, 128, True, False),  # pieces of about 128 key tiles
+    "mla_noncausal_ragged": (1, 2, 2, 3000, 192, False, False),  # every item split, ragged S
 }
 
 
