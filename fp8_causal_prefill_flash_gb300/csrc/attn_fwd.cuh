@@ -1035,7 +1035,7 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
           __threadfence();
           // every piece from the workspace (this one's too), in piece order,
           // rescaled to the largest reference: the output straight from the
-          // sums, four columns at a time (no 128-value array in registers)
+          // sums, 32 columns at a time (no 128-value array in registers)
           float R = -INFINITY;
 #pragma unroll
           for (int s = 0; s < 4; ++s)
