@@ -211,3 +211,26 @@ def test_split_call_replays_from_a_cuda_graph():
         want = fa.attn_fwd_full(variant, *src, causal=causal)
         torch.cuda.synchronize()
         assert torch.equal(out, want)
+
+
+def test_split_kernel_reports_a_stall_and_the_next_call_is_correct():
+    """Test hook: the load warp issues nothing, every bounded wait of the split
+    kernel expires (0.2 s) and the status word reads ATTN_ERR_TIMEOUT; the next
+    call on the same workspace is correct (no piece arrived, so no counter
+    moved, and the next call's tag differs anyway)."""
+    variant = fa.ATTN_VARIANT_LEANP
+    case, args, _, causal = make("h8_s2048", 600)
+    need = fa.workspace_size(variant, *case.shape, causal)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fa.attn_fwd_full(variant, *args, causal=causal, flags=fa.ATTN_FLAG_TEST_STALL_LOADS,
+                     dev_status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.ATTN_ERR_TIMEOUT
+    status.zero_()
+    out, _ = call(variant, args, causal, workspace=ws, status=status)
+    plain, _ = call(variant, args, causal, split=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.ATTN_OK
+    assert float((out - plain).abs().max()) <= 2e-6 * float(plain.abs().max())
