@@ -30,7 +30,7 @@ Key 4 and key 66 pin the ceiling of the block exponent and the constants:
 a floor or a rounded exponent, or T = 8 with C = 120, moves them out of the
 subnormal range and changes their weights (normal codes are compensated).
 
-Running-maximum anchoring (the survey's reading, oracle path "leanp_a3"):
+Running-maximum anchoring (the second reading of the block scale, oracle path "leanp_a3"):
 one 128-key tile, m = 20.5 for every row, k = floor((m - block max)/8),
 code = clamp(floor(u - m + 8k + 112 + 1/64), 0, 126), weight relative to
 2^(m/8) = dec(code) * 2^(-7-k):

@@ -21,8 +21,8 @@ target:
    by sigma times its own RMS.  On the headline workload's distribution
    (N(0,1) inputs, per-tensor e4m3, d = 128) rows with 16K and 24K keys
    therefore sit at about 3.1e-2 under both anchorings of the code grid
-   (integer binades, the library's reading, and the running maximum, the
-   survey's), above the 3e-2 target, and the ablation at about 2.6e-2.
+   (integer binades, the product's reading, and the running maximum, the
+   second reading), above the 3e-2 target, and the ablation at about 2.6e-2.
    Neither anchoring can bring such rows under 3e-2.
 3. The target applies to the whole output, and there the short rows weigh
    heavily: row i's output has a size of about |v| / sqrt(i), so the rows
