@@ -823,8 +823,8 @@ print(json.dumps(res))
 
 def run_cpu_sweep(args):
     """The oracle on the host cores: every configuration on a bounded sample
-    of rows (the pass the GPU computes, ref_fp64 and emul_leanp), and C1 in
-    full on one core (a child process with OMP_NUM_THREADS=1)."""
+    of rows (the pass the GPU computes, ref_fp64 and emul_leanp), and the
+    2-head 256-key case (fp8_h2_s256_d128) in full on one core (a child process with OMP_NUM_THREADS=1)."""
     from fp8_causal_prefill_flash_gb300 import workloads as wl
     import oracle
     oracle.build()
@@ -1062,8 +1062,8 @@ def main():
     ap.add_argument("--only", choices=list(ONLY_PATHS), default=None,
                     help="time one kernel alone on its workload (profiling)")
     ap.add_argument("--cpu-sweep", action="store_true",
-                    help="time the oracle on every configuration (bounded samples) and C1 "
-                         "in full on one core")
+                    help="time the oracle on every configuration (bounded samples) and the "
+                         "2-head 256-key case in full on one core")
     ap.add_argument("--sweep", action="store_true",
                     help="time every path on every configuration, one JSON line each")
     ap.add_argument("--clock-study", action="store_true",

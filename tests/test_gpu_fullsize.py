@@ -211,7 +211,7 @@ def test_bf16_fullsize():
 
 
 def test_noncausal_fullsize_with_per_bkv_descales():
-    """The non-causal call the sweep times on the C2 shape (every row sees all
+    """The non-causal call the sweep times on the 16K GQA shape (every row sees all
     S keys), here with descales per (batch, kv head): Lean-P output and LSE
     against the oracle's non-causal definition on sampled rows."""
     case = wl.make_case("fp8_gqa_h32_8_s16k_d128_outliers")
