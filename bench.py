@@ -490,7 +490,7 @@ def run_ours(args, rank, world, local_rank):
         fa.attn_fwd_fp8(q, k, v, *d, out=out)
         hout.copy_(out, non_blocking=True)
     # at least 20 steps: a short pipelined run is dominated by filling it
-    n_e2e = max(50, args.steps // 10)  # the pipeline's fill and drain amortised over 50 steps
+    n_e2e = max(20, args.steps // 10)
     ms_e2e_serial = timed(step_e2e_serial, n_e2e, 4)
     # Pipelined (a serving loop): two device buffer sets; the upload of step
     # i+1 (copy stream) and the download of step i-1 (second copy stream)
