@@ -136,8 +136,9 @@ size_t split_ws_bytes(int n_split_items, int ns) {
 // per key tile of both query tiles `step`, per unit `unit_cost` (the item
 // boundary), per piece `piece_cost` (its partial result written, and the ns
 // partial results read and added up by the last piece).  The constants are a
-// least-squares fit to GB300 times of 100 forced plans (2 to 16 heads, 2K to
-// 8K keys, head dims 128 and 192; the model's time is within 10% of each).
+// least-squares fit to GB300 times of 103 forced plans (2 to 16 heads, 2K to
+// 8K keys, head dims 128 and 192; with 5 us for the launch, the model's time
+// is within 8% of each).
 long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal, int Dqk, int sq,
                          int ns, int grid, std::vector<long long>& load) {
   const long long step = Dqk == 192 ? 1140 : 950, unit_cost = 5000;
