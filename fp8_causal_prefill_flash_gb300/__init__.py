@@ -296,8 +296,8 @@ def attn_quantize_fp8(x, hadamard=False, codes=None, descale=None):
 def workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal=True, flags=0) -> int:
     """Bytes of workspace ``attn_fwd_full`` uses on the current device for
     these arguments (``attn_workspace_size`` of the C ABI): 0 unless the
-    problem has too few work items to fill the SMs and the variant's codes
-    depend on each key block alone (Lean-P, block-exact)."""
+    problem has too few work items to fill the SMs and the variant splits
+    (Lean-P, block-exact and BF16)."""
     n = ctypes.c_size_t(0)
     st = load_library().attn_workspace_size(int(variant), B, Hq, Hkv, S, Dqk, Dv,
                                             int(bool(causal)), int(flags), ctypes.byref(n))

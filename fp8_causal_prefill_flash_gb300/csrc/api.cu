@@ -139,9 +139,9 @@ size_t split_ws_bytes(int n_split_items, int ns) {
 // least-squares fit to GB300 times of 103 forced plans (2 to 16 heads, 2K to
 // 8K keys, head dims 128 and 192; with 5 us for the launch, the model's time
 // is within 8% of each).
-long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal, int Dqk, int sq,
+long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal, int step, int sq,
                          int ns, int grid, std::vector<long long>& load) {
-  const long long step = Dqk == 192 ? 1140 : 950, unit_cost = 5000;
+  const long long unit_cost = 5000;
   const long long piece_cost = 3000 + 1000 * ns;
   load.assign(grid, 0);
   long long pos = 0;
@@ -174,13 +174,13 @@ long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal
 // The split schedule for a problem (none unless it helps by 5% or more in the
 // model above: smaller predicted gains are within the model's error).  Plans
 // are cached: the search walks every candidate.
-SplitPlan split_plan(int units_bh, int S, int causal, int Dqk, int sms, size_t limit) {
+SplitPlan split_plan(int units_bh, int S, int causal, int step, int sms, size_t limit) {
   SplitPlan best;
   const int n_qblocks = (S + 255) / 256, n_kv_tiles = (S + 127) / 128;
   const long long n_items = (long long)units_bh * n_qblocks;
   if (n_items >= (long long)kSplitMaxWaves * sms) return best;
   struct Entry {
-    int units_bh, S, causal, Dqk, sms;
+    int units_bh, S, causal, step, sms;
     size_t limit;
     SplitPlan plan;
   };
@@ -189,14 +189,14 @@ SplitPlan split_plan(int units_bh, int S, int causal, int Dqk, int sms, size_t l
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry& e : cache)
-      if (e.units_bh == units_bh && e.S == S && e.causal == causal && e.Dqk == Dqk &&
+      if (e.units_bh == units_bh && e.S == S && e.causal == causal && e.step == step &&
           e.sms == sms && e.limit == limit)
         return e.plan;
   }
   std::vector<long long> load;
   const int grid0 = (int)(n_items < sms ? n_items : sms);
   const long long base =
-      split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, Dqk, 0, 1, grid0, load);
+      split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, step, 0, 1, grid0, load);
   long long best_t = base;
   for (int ns = 2; ns <= 4; ++ns)
     for (int sq = n_qblocks - 1; sq >= 0; --sq) {
@@ -208,7 +208,7 @@ SplitPlan split_plan(int units_bh, int S, int causal, int Dqk, int sms, size_t l
       const long long n_units = n_items + (long long)n_split * (ns - 1);
       const int grid = (int)(n_units < sms ? n_units : sms);
       const long long t =
-          split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, Dqk, sq, ns, grid, load);
+          split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, step, sq, ns, grid, load);
       if (t < best_t) {
         best_t = t;
         best.split_qb = sq;
@@ -220,7 +220,7 @@ SplitPlan split_plan(int units_bh, int S, int causal, int Dqk, int sms, size_t l
   if (best.n_split_items > 0 && best_t * 100 > base * 95) best = SplitPlan();
   std::lock_guard<std::mutex> lk(mu);
   if (cache.size() >= 64) cache.erase(cache.begin());
-  cache.push_back({units_bh, S, causal, Dqk, sms, limit, best});
+  cache.push_back({units_bh, S, causal, step, sms, limit, best});
   return best;
 }
 
@@ -235,7 +235,16 @@ unsigned long long next_epoch() {
 }
 
 bool split_variant(int variant) {
-  return variant == ATTN_VARIANT_LEANP || variant == ATTN_VARIANT_BLOCK_EXACT;
+  return variant == ATTN_VARIANT_LEANP || variant == ATTN_VARIANT_BLOCK_EXACT ||
+         variant == ATTN_VARIANT_BF16;
+}
+
+// The model's time per key tile of both query tiles (ns at about 2 GHz): the
+// fitted Lean-P figure, scaled by the measured throughput of the MLA shape
+// and of the BF16 path relative to Lean-P at head dim 128.
+int split_step(int variant, int Dqk) {
+  if (variant == ATTN_VARIANT_BF16) return 1500;
+  return Dqk == 192 ? 1140 : 950;
 }
 
 int run(int variant, const void* q, const void* k, const void* v, const float* dq, const float* dk,
@@ -314,7 +323,7 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   // key block alone, in the plain (unchunked) item order.
   SplitPlan plan;
   if (workspace && split_variant(variant) && p.chunk_q == B * Hq)
-    plan = split_plan(B * Hq, S, causal, Dqk, sms, kSplitMaxBytes);
+    plan = split_plan(B * Hq, S, causal, split_step(variant, Dqk), sms, kSplitMaxBytes);
   if (plan.n_split_items > 0 && workspace_bytes < plan.ws_bytes) return ATTN_ERR_INVALID_ARG;
   p.split_qb = plan.split_qb;
   p.split_ns = plan.ns;
@@ -353,6 +362,7 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (split) {
+    if (variant == ATTN_VARIANT_BF16) return launch<fa8::kBf16, 128, true>(maps, p, sms, s);
     if (variant == ATTN_VARIANT_LEANP)
       return Dqk == 128 ? launch<fa8::kLeanP, 128, true>(maps, p, sms, s)
                         : launch<fa8::kLeanP, 192, true>(maps, p, sms, s);
@@ -432,12 +442,12 @@ int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int
   if (n_items > (1ll << 30) || (long long)B * S > (1ll << 31)) return ATTN_ERR_INVALID_ARG;
   if (!split_variant(variant) || (flags & ATTN_FLAG_TEST_CHUNK_UNITS)) return ATTN_OK;
   // only the unchunked item order splits (see run)
-  const size_t kv_unit = (size_t)S * (size_t)(Dqk + Dv);
+  const size_t kv_unit = (size_t)S * (size_t)(Dqk + Dv) * (variant == ATTN_VARIANT_BF16 ? 2 : 1);
   if (kv_unit * (size_t)((long long)B * Hkv) > kChunkAllBytes) return ATTN_OK;
   int sms = 0;
   const int st = device_check(&sms);
   if (st != ATTN_OK) return st;
-  *bytes = split_plan(B * Hq, S, causal, Dqk, sms, kSplitMaxBytes).ws_bytes;
+  *bytes = split_plan(B * Hq, S, causal, split_step(variant, Dqk), sms, kSplitMaxBytes).ws_bytes;
   return ATTN_OK;
 }
 

@@ -988,6 +988,153 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
     const float ref2 = V == kLeanPA3 ? ref * lam : ref;
     // row sum l (relative to 2^ref): Lean-P paths, the scaled rounded weights
     // in O's row-sum column; exact paths, the unrounded p summed on the cores
+    if constexpr (SPLIT) {
+      // the piece is worked out again from the unit index here, so that the
+      // key-tile loop carries one register for it instead of three
+      const int ns = p.split_ns, sidx = w.u / ns, piece = w.u - sidx * ns;
+      if (w.u < p.n_split_items * ns) {
+        // One piece of a split item: O, l and ref (O and l relative to 2^ref)
+        // go to the workspace and O_t is released; the piece that arrives
+        // last adds the pieces up in piece order, rescaled to the largest
+        // ref (Lean-P: integer binades, so the rescale is an exact power of
+        // two; BF16: the running maxima, exp2 of their difference), so the
+        // sum does not depend on which piece it is, and writes the output.
+        // The others are done with this unit.
+        float lt = l;  // exact paths: the unrounded row sum in registers
+        if constexpr (C::kBlockScaled) lt = __uint_as_float(tmem_ld1_wait(o_col + 128));
+        float* slots = reinterpret_cast<float*>(p.ws + split_cnt_bytes(p.n_split_items));
+        auto slot = [&](int s_) {
+          return slots + ((size_t)(sidx * ns + s_) * 2 + t) * kSplitSlotFloats;
+        };
+        float* mine = slot(piece);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // O in 32-column chunks
+          uint32_t o[32];
+          tmem_ld32_wait(o_col + 32 * c, o);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(reinterpret_cast<float4*>(mine) + (8 * c + i) * 128 + r,
+                   make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                               __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])));
+        }
+        tc_fence_before();
+        mbar_arrive(&bars.o_free[t]);
+        __stcg(mine + 128 * 128 + r, lt);
+        __stcg(mine + 128 * 129 + r, ref2);
+        __threadfence();
+        // the tile's four warps: every row's partial is written and fenced
+        // (an mbarrier, so that the wait is bounded like every other)
+        auto group_sync = [&]() {
+          mbar_arrive(&bars.split_sync[t]);
+          return warp_wait(&bars.split_sync[t], (sync_cnt++) & 1, ab, lim);
+        };
+        if (!group_sync()) return;
+        if (r == 0) bars.split_last[t] = split_arrive(p, sidx, ns, t, ab) ? 1 : 0;
+        if (!group_sync()) return;
+        if (!bars.split_last[t]) continue;
+        __threadfence();
+        // every piece from the workspace (this one's too), in piece order,
+        // rescaled to the largest reference: the output straight from the
+        // sums, 32 columns at a time (no 128-value array in registers)
+        float R = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (s < ns) R = fmaxf(R, __ldcg(slot(s) + 128 * 129 + r));
+        float sc[4];
+        float L = 0.0f;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          sc[s] = 0.0f;
+          if (s < ns) {
+            const float d = __ldcg(slot(s) + 128 * 129 + r) - R;  // <= 0 (Lean-P: integers)
+            if constexpr (C::kBlockScaled)
+              sc[s] = d < -126.0f ? 0.0f : pow2i((int)d);
+            else
+              sc[s] = exp2f(d);
+            L = fmaf(__ldcg(slot(s) + 128 * 128 + r), sc[s], L);
+          }
+        }
+        const float inv = dvv / L;
+        if (p.lse && store)
+          p.lse[((size_t)b * p.Hq + h) * p.S + row] = (R + log2f(L)) * 0.6931471805599453f;
+        // 32 output columns at a time: every piece's values are loaded
+        // before any of the group's stores, so the loads of a group are in
+        // flight together instead of waiting behind stores that might alias
+        auto sum32 = [&](int g, float (&y)[32]) {  // columns 32g .. 32g+31
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = 0.0f;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            if (s < ns) {
+              float4 x[8];
+              const float4* src = reinterpret_cast<const float4*>(slot(s)) + (8 * g) * 128 + r;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + i * 128);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                y[4 * i] = fmaf(x[i].x, sc[s], y[4 * i]);
+                y[4 * i + 1] = fmaf(x[i].y, sc[s], y[4 * i + 1]);
+                y[4 * i + 2] = fmaf(x[i].z, sc[s], y[4 * i + 2]);
+                y[4 * i + 3] = fmaf(x[i].w, sc[s], y[4 * i + 3]);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] *= inv;
+        };
+        auto bf16x8 = [&](const float (&y)[32], int c) {  // y[8c .. 8c+7] as eight bf16
+          uint32_t w4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 hv = __floats2bfloat162_rn(y[8 * c + 2 * k], y[8 * c + 2 * k + 1]);
+            w4[k] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          return make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        };
+        if (C::kEpiTma && !p.out_f32) {
+          // as the whole-item epilogue below: this warp's slot, TMA stores
+          uint8_t* oslot = smem + C::kSmemOut + (t * 4 + quad) * C::kOutSlotBytes;
+          const int row0 = qb * 256 + t * 128 + (int)quad * 32;
+          const uint32_t lane = lane_id();
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            float y0[32], y1[32];
+            sum32(2 * half, y0);
+            sum32(2 * half + 1, y1);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              *reinterpret_cast<uint4*>(oslot + lane * 128 + ((c ^ (lane & 7)) * 16)) = bf16x8(y0, c);
+              *reinterpret_cast<uint4*>(oslot + lane * 128 + (((c + 4) ^ (lane & 7)) * 16)) =
+                  bf16x8(y1, c);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < p.S) {
+              tma_store_4d(&maps.o64, oslot, 64 * half, h, row0, b);
+              bulk_commit();
+            }
+          }
+        } else if (store) {
+#pragma unroll 1
+          for (int g = 0; g < 4; ++g) {
+            float y[32];
+            sum32(g, y);
+            if (p.out_f32) {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV) + 8 * g;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV) + 4 * g;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) dst[c] = bf16x8(y, c);
+            }
+          }
+        }
+        continue;
+      }
+    }
     if constexpr (C::kEarlyOFree) {
       // O_t (and its row-sum column) in registers with one wait, then O_t is
       // released before the stores, so the next item's first P.V product
@@ -999,139 +1146,6 @@ __device__ void softmax_loop(const KParams& p, const Maps& maps, uint8_t* smem, 
       mbar_arrive(&bars.o_free[t]);
       if (r == 0) FA8_TL(5, round, 4 * t + 2);
       if constexpr (C::kBlockScaled) l = __uint_as_float(lsum);
-      if constexpr (SPLIT) {
-        // the piece is worked out again from the unit index here, so that
-        // the key-tile loop carries one register for it instead of three
-        const int ns = p.split_ns, sidx = w.u / ns, piece = w.u - sidx * ns;
-        if (w.u < p.n_split_items * ns) {
-          // One piece of a split item: O, l and ref (O and l relative to
-          // 2^ref) go to the workspace; the piece that arrives last adds the
-          // pieces up in piece order (exact power-of-two rescales to the
-          // largest ref), so the sum does not depend on which piece it is,
-          // and writes the output.  The others are done with this unit.
-          float* slots = reinterpret_cast<float*>(p.ws + split_cnt_bytes(p.n_split_items));
-          auto slot = [&](int s) {
-            return slots + ((size_t)(sidx * ns + s) * 2 + t) * kSplitSlotFloats;
-          };
-          float* mine = slot(piece);
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            __stcg(reinterpret_cast<float4*>(mine) + c * 128 + r,
-                   make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                               __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3])));
-          __stcg(mine + 128 * 128 + r, l);
-          __stcg(mine + 128 * 129 + r, ref2);
-          __threadfence();
-          // the tile's four warps: every row's partial is written and fenced
-          // (an mbarrier, so that the wait is bounded like every other)
-          auto group_sync = [&]() {
-            mbar_arrive(&bars.split_sync[t]);
-            return warp_wait(&bars.split_sync[t], (sync_cnt++) & 1, ab, lim);
-          };
-          if (!group_sync()) return;
-          if (r == 0) bars.split_last[t] = split_arrive(p, sidx, ns, t, ab) ? 1 : 0;
-          if (!group_sync()) return;
-          if (!bars.split_last[t]) continue;
-          __threadfence();
-          // every piece from the workspace (this one's too), in piece order,
-          // rescaled to the largest reference: the output straight from the
-          // sums, 32 columns at a time (no 128-value array in registers)
-          float R = -INFINITY;
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            if (s < ns) R = fmaxf(R, __ldcg(slot(s) + 128 * 129 + r));
-          float sc[4];
-          float L = 0.0f;
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            sc[s] = 0.0f;
-            if (s < ns) {
-              const float d = __ldcg(slot(s) + 128 * 129 + r) - R;  // integers: exact, <= 0
-              sc[s] = d < -126.0f ? 0.0f : pow2i((int)d);
-              L = fmaf(__ldcg(slot(s) + 128 * 128 + r), sc[s], L);
-            }
-          }
-          const float inv = dvv / L;
-          if (p.lse && store)
-            p.lse[((size_t)b * p.Hq + h) * p.S + row] = (R + log2f(L)) * 0.6931471805599453f;
-          // 32 output columns at a time: every piece's values are loaded
-          // before any of the group's stores, so the loads of a group are in
-          // flight together instead of waiting behind stores that might alias
-          auto sum32 = [&](int g, float (&y)[32]) {  // columns 32g .. 32g+31
-#pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] = 0.0f;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              if (s < ns) {
-                float4 x[8];
-                const float4* src = reinterpret_cast<const float4*>(slot(s)) + (8 * g) * 128 + r;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = __ldcg(src + i * 128);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  y[4 * i] = fmaf(x[i].x, sc[s], y[4 * i]);
-                  y[4 * i + 1] = fmaf(x[i].y, sc[s], y[4 * i + 1]);
-                  y[4 * i + 2] = fmaf(x[i].z, sc[s], y[4 * i + 2]);
-                  y[4 * i + 3] = fmaf(x[i].w, sc[s], y[4 * i + 3]);
-                }
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) y[i] *= inv;
-          };
-          auto bf16x8 = [&](const float (&y)[32], int c) {  // y[8c .. 8c+7] as eight bf16
-            uint32_t w4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              __nv_bfloat162 hv = __floats2bfloat162_rn(y[8 * c + 2 * k], y[8 * c + 2 * k + 1]);
-              w4[k] = *reinterpret_cast<uint32_t*>(&hv);
-            }
-            return make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          };
-          if (C::kEpiTma && !p.out_f32) {
-            // as the whole-item epilogue below: this warp's slot, TMA stores
-            uint8_t* oslot = smem + C::kSmemOut + (t * 4 + quad) * C::kOutSlotBytes;
-            const int row0 = qb * 256 + t * 128 + (int)quad * 32;
-            const uint32_t lane = lane_id();
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              float y0[32], y1[32];
-              sum32(2 * half, y0);
-              sum32(2 * half + 1, y1);
-              if (lane == 0) bulk_wait_read_all();
-              __syncwarp();
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                *reinterpret_cast<uint4*>(oslot + lane * 128 + ((c ^ (lane & 7)) * 16)) = bf16x8(y0, c);
-                *reinterpret_cast<uint4*>(oslot + lane * 128 + (((c + 4) ^ (lane & 7)) * 16)) =
-                    bf16x8(y1, c);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0 && row0 < p.S) {
-                tma_store_4d(&maps.o64, oslot, 64 * half, h, row0, b);
-                bulk_commit();
-              }
-            }
-          } else if (store) {
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-              float y[32];
-              sum32(g, y);
-              if (p.out_f32) {
-                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kDV) + 8 * g;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDV) + 4 * g;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) dst[c] = bf16x8(y, c);
-              }
-            }
-          }
-          continue;
-        }
-      }
       const float inv = dvv / l;
       if (p.lse && store)
         p.lse[((size_t)b * p.Hq + h) * p.S + row] = (ref2 + log2f(l)) * 0.6931471805599453f;
@@ -1240,8 +1254,12 @@ template <int V, int DQK, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ Maps maps, const KParams p) {
   using C = Cfg<V, DQK>;
-  // the split schedule needs codes that depend on each 64-key block alone
-  static_assert(!SPLIT || V == kLeanP || V == kBlockExact, "split units: block-local codes only");
+  // the split schedule: Lean-P and block-exact, whose codes depend on each
+  // 64-key block alone (a split changes only the order of the fp32 sums),
+  // and BF16, whose probabilities are rounded relative to each piece's own
+  // running maximum (within the rounding of bf16)
+  static_assert(!SPLIT || V == kLeanP || V == kBlockExact || V == kBf16,
+                "split units: block-local codes or bf16 probabilities");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

@@ -208,11 +208,14 @@ int attn_launches_per_call(void);
  *              With it, problems with too few work items to fill every SM
  *              (few heads, short sequences) split their longest items along
  *              the keys into pieces that run on different SMs and are added up
- *              by the piece that finishes last (ATTN_VARIANT_LEANP and
- *              ATTN_VARIANT_BLOCK_EXACT, whose codes depend on each 64-key
- *              block alone, so a split changes only the order of the fp32
- *              sums; the pieces are added in a fixed order, so the result is
- *              the same on every call).  The memory needs no clearing: it holds
+ *              by the piece that finishes last, in a fixed order, so the result
+ *              is the same on every call.  ATTN_VARIANT_LEANP and
+ *              ATTN_VARIANT_BLOCK_EXACT: the codes depend on each 64-key block
+ *              alone, so a split changes only the order of the fp32 sums.
+ *              ATTN_VARIANT_BF16: each piece rounds its probabilities to bf16
+ *              relative to its own running maximum, so a split result differs
+ *              from whole items within the rounding of bf16.  The other
+ *              variants always run whole items.  The memory needs no clearing: it holds
  *              partial results and counters tagged with a per-call number.
  *              Too small a workspace is an ATTN_ERR_INVALID_ARG; NULL runs
  *              every item whole, as attn_fwd_ex does.
@@ -227,7 +230,7 @@ int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
 /*
  * Bytes of workspace attn_fwd_full uses for these arguments on the CURRENT
  * device (its SM count enters the schedule): 0 when the problem runs without
- * splitting (enough work items, another variant, or
+ * splitting (enough work items, a variant that does not split, or
  * ATTN_FLAG_TEST_CHUNK_UNITS), otherwise at most 128 MiB.  The split
  * schedule is chosen by a model of the kernel's time per key tile and per
  * work unit; it is cached per shape.  Returns an attn_status; *bytes is 0 on

@@ -121,15 +121,16 @@ def test_full_entry_point_checks_arguments(lib):
 
 def test_workspace_size_query(lib):
     """attn_workspace_size: argument errors, and 0 (no split, no device
-    needed) for the variants whose codes depend on the running maximum and
-    for problems whose K and V are large enough for the chunked order."""
+    needed) for the variants that never split (the running-maximum anchor and
+    the exact-FP8 ablation) and for problems whose K and V are large enough
+    for the chunked order."""
     n = ctypes.c_size_t(123)
     q = lambda *a, **kw: lib.attn_workspace_size(*a, ctypes.byref(n))
     assert lib.attn_workspace_size(0, 1, 2, 2, 128, 128, 128, 1, 0, None) == fa.ATTN_ERR_INVALID_ARG
     assert q(0, 1, 3, 2, 128, 128, 128, 1, 0) == fa.ATTN_ERR_INVALID_ARG and n.value == 0  # Hq % Hkv
     assert q(9, 1, 2, 2, 128, 128, 128, 1, 0) == fa.ATTN_ERR_INVALID_ARG                 # variant
     assert q(0, 1, 2, 2, 128, 128, 128, 2, 0) == fa.ATTN_ERR_INVALID_ARG                 # causal
-    for variant in (fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_BF16, fa.ATTN_VARIANT_LEANP_A3):
+    for variant in (fa.ATTN_VARIANT_EXACT_FP8, fa.ATTN_VARIANT_LEANP_A3):
         n.value = 123
         assert q(variant, 1, 8, 8, 4096, 128, 128, 1, 0) == fa.ATTN_OK and n.value == 0
     n.value = 123
@@ -137,6 +138,9 @@ def test_workspace_size_query(lib):
     assert n.value == 0
     n.value = 123
     assert q(0, 1, 32, 32, 65536, 128, 128, 1, 0) == fa.ATTN_OK and n.value == 0      # chunked
+    n.value = 123
+    assert q(fa.ATTN_VARIANT_BF16, 1, 16, 16, 65536, 128, 128, 1, 0) == fa.ATTN_OK  # bf16 K, V:
+    assert n.value == 0                                                   # 2 bytes each
 
 
 def test_release_library_has_no_timeline(lib):

@@ -234,3 +234,54 @@ def test_split_kernel_reports_a_stall_and_the_next_call_is_correct():
     torch.cuda.synchronize()
     assert int(status.item()) == fa.ATTN_OK
     assert float((out - plain).abs().max()) <= 2e-6 * float(plain.abs().max())
+
+
+# BF16 (exact softmax): each piece rounds its probabilities to bf16 relative
+# to its own running maximum, and the last piece rescales the pieces by exp2
+# of their maxima's differences, so a split result differs from whole items
+# by that rounding.  Where every probability is rounded differently on the
+# two sides, the difference is two independent round-to-nearest errors of
+# relative size up to 2^-9 each, weighted like the output itself: for values
+# that average out (the non-causal rows over 2000 keys) its RMS relative to
+# the output's RMS is about sqrt(2/3) * 2^-9 = 1.6e-3.  The test allows twice
+# one rounding step, 2^-8, and the gate against fp64 (5e-3) still applies.
+BF16_SHAPES = {
+    "h8_s2048": (1, 8, 8, 2048, True),
+    "gqa_b2_ragged": (2, 8, 2, 1500, True),
+    "noncausal_h4": (1, 4, 4, 2000, False),
+    "h2_s4096": (1, 2, 2, 4096, True),
+}
+
+
+@pytest.mark.parametrize("name", list(BF16_SHAPES))
+def test_bf16_split_against_fp64_and_whole_items(name):
+    B, Hq, Hkv, S, causal = BF16_SHAPES[name]
+    case = wl.bf16_gaussian_case(B, Hq, Hkv, S, 128, 128, seeds=(700, 701, 702))
+    q, k, v = (torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+               for a in (case.q, case.k, case.v))
+    variant = fa.ATTN_VARIANT_BF16
+    assert fa.workspace_size(variant, B, Hq, Hkv, S, 128, 128, causal) > 0
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = fa.attn_fwd_full(variant, q, k, v, out_dtype=fa.ATTN_OUT_F32, causal=causal,
+                                return_lse=True, dev_status=status)
+    plain, plain_lse = fa.attn_fwd_full(variant, q, k, v, out_dtype=fa.ATTN_OUT_F32,
+                                        causal=causal, return_lse=True, split=False)
+    again = fa.attn_fwd_full(variant, q, k, v, out_dtype=fa.ATTN_OUT_F32, causal=causal)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.ATTN_OK
+    assert torch.equal(out, again)  # the same bits on every call
+    scale = float(plain.abs().max())
+    diff = (out - plain).double()
+    assert float(diff.abs().max()) <= 4e-3 * scale
+    assert float(diff.pow(2).mean().sqrt()) <= 2.0 ** -8 * float(plain.double().pow(2).mean().sqrt())
+    assert float((lse - plain_lse).abs().max()) <= 1e-3 * (1.0 + float(plain_lse.abs().max()))
+    rows = sample_rows(B, Hq, S, 703, n=500)
+    ref, _, ref_lse = oracle.attention("ref_bf16", case.q, case.k, case.v, rows=rows,
+                                       causal=causal)
+    gpu = out.cpu().numpy().astype(np.float64)
+    got = np.stack([gpu[b, i, h] for b, h, i in rows])
+    rel = float(np.sqrt(np.mean((got - ref) ** 2)) / np.sqrt(np.mean(ref ** 2)))
+    assert rel <= 5e-3, rel
+    emul, _, _ = oracle.attention("bf16", case.q, case.k, case.v, rows=rows, causal=causal)
+    vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
+    check_rows(got, emul, np.zeros(len(rows)), vmax)
