@@ -647,30 +647,38 @@ def extra_legs(torch, fa, wl, dev, stream, timed, peaks, sms, n):
         del q, k, v, o
         torch.cuda.empty_cache()
     legs["leanp_few_heads_split"] = split_leg(torch, fa, wl, dev, peaks, n)
+    legs["bf16_few_heads_split"] = split_leg(torch, fa, wl, dev, peaks, n, bf16=True)
     return legs
 
 
-def split_leg(torch, fa, wl, dev, peaks, n):
-    """Lean-P on few heads (fp8_h4_s8k_d128: 128 work items for the SMs),
-    with the split schedule (attn_fwd_full and a workspace) and with whole
-    items.  The inputs fit in L2, so a 256 MB buffer is written before every
-    timed call and only the call is timed."""
-    name = "fp8_h4_s8k_d128"
+def split_leg(torch, fa, wl, dev, peaks, n, bf16=False):
+    """Few heads (4 heads at 8K keys: 128 work items for the SMs), Lean-P on
+    fp8_h4_s8k_d128 or BF16 on bf16_h4_s8k_d128, with the split schedule
+    (attn_fwd_full and a workspace) and with whole items.  The inputs fit in
+    L2, so a 256 MB buffer is written before every timed call and only the
+    call is timed."""
+    name = "bf16_h4_s8k_d128" if bf16 else "fp8_h4_s8k_d128"
+    variant = fa.ATTN_VARIANT_BF16 if bf16 else fa.ATTN_VARIANT_LEANP
     case = wl.make_case(name)
     B, Hq, Hkv, S, Dqk, Dv = case.shape
     F = causal_flops(B, Hq, S, Dqk, Dv)
-    q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
-    d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
+    if bf16:
+        q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+                   for a in (case.q, case.k, case.v))
+        d = [None, None, None]
+    else:
+        q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
+        d = [torch.tensor([x], dtype=torch.float32, device=dev)
+             for x in (case.dq, case.dk, case.dv)]
     o = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
-    need = fa.workspace_size(fa.ATTN_VARIANT_LEANP, B, Hq, Hkv, S, Dqk, Dv, True)
+    need = fa.workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, True)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     n = max(n, 40)  # short calls: enough of them to average out the event resolution
     out = {"workload": name, "unit": "TFLOP/s", "workspace_bytes": need, "steps": n,
            "l2": "256 MB written before every timed call",
            "order": "split and whole calls alternate"}
-    fns = {key: (lambda split=split: fa.attn_fwd_full(fa.ATTN_VARIANT_LEANP, q, k, v, *d, out=o,
-                                                       split=split,
+    fns = {key: (lambda split=split: fa.attn_fwd_full(variant, q, k, v, *d, out=o, split=split,
                                                        workspace=ws if need else None))
            for key, split in (("split", True), ("whole", False))}
     for fn in fns.values():
@@ -689,7 +697,7 @@ def split_leg(torch, fa, wl, dev, peaks, n):
     for key in fns:
         ms = total[key] / n
         out[key] = {"value": F / (ms * 1e-3) / 1e12, "ms_per_step": ms}
-    peak = peaks["bf16_burst"] * FP8_OVER_BF16
+    peak = peaks["bf16_burst"] * (1.0 if bf16 else FP8_OVER_BF16)
     out["value"] = out["split"]["value"]
     out["frac"] = out["value"] / peak
     out["speedup_over_whole_items"] = out["split"]["value"] / out["whole"]["value"]

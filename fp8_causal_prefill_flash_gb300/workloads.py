@@ -156,6 +156,8 @@ CONFIGS = {
     # few heads: one tensor-parallel shard of a larger model (fewer work items than SMs)
     "fp8_h4_s8k_d128": dict(kind="fp8", B=1, Hq=4, Hkv=4, S=8192, Dqk=128, Dv=128,
                             seeds=(60, 61, 62)),
+    "bf16_h4_s8k_d128": dict(kind="bf16", B=1, Hq=4, Hkv=4, S=8192, Dqk=128, Dv=128,
+                             seeds=(63, 64, 65)),
     # stress input: an attention sink at key 0 (+15..25 nats, varying per row), V mean 1
     "fp8_sink_h8_s8k_d128": dict(kind="fp8_sink", B=1, Hq=8, Hkv=8, S=8192, Dqk=128, Dv=128,
                                  seeds=(50, 51, 52)),
