@@ -130,19 +130,36 @@ size_t split_ws_bytes(int n_split_items, int ns) {
          (size_t)n_split_items * ns * 2 * fa8::kSplitSlotFloats * sizeof(float);
 }
 
+// The plan model's costs (ns at about 2 GHz): per key tile of both query
+// tiles, per unit (the item boundary), and per piece piece0 + piece_ns * ns
+// (its partial result written, and the ns partial results read and added up
+// by the last piece).
+struct SplitCosts {
+  int step, unit, piece0, piece_ns;
+  bool operator==(const SplitCosts& o) const {
+    return step == o.step && unit == o.unit && piece0 == o.piece0 && piece_ns == o.piece_ns;
+  }
+};
+
+// Least-squares fits to GB300 times of forced plans.  FP8 (Lean-P, and
+// block-exact alike): 103 plans on 2 to 16 heads, 2K to 8K keys, head dims 128
+// and 192, within 8% of each with 5 us for the launch; the MLA shape's step
+// is the head-dim-128 step scaled by its measured throughput.  BF16: 180
+// plans on 1 to 16 heads, 1K to 16K keys, causal and not, within 7.4% of each
+// with 3 us for the launch.
+SplitCosts split_costs(int variant, int Dqk) {
+  if (variant == ATTN_VARIANT_BF16) return {1580, 6640, 5360, 1300};
+  return {Dqk == 192 ? 1140 : 950, 5000, 3000, 1000};
+}
+
 // Estimated finishing time of the busiest CTA (ns) when the items of query
 // block >= sq are split into ns pieces (ns = 1: no split), following the
-// kernel's unit order and its alternating round-robin assignment (item_at):
-// per key tile of both query tiles `step`, per unit `unit_cost` (the item
-// boundary), per piece `piece_cost` (its partial result written, and the ns
-// partial results read and added up by the last piece).  The constants are a
-// least-squares fit to GB300 times of 103 forced plans (2 to 16 heads, 2K to
-// 8K keys, head dims 128 and 192; with 5 us for the launch, the model's time
-// is within 8% of each).
-long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal, int step, int sq,
-                         int ns, int grid, std::vector<long long>& load) {
-  const long long unit_cost = 5000;
-  const long long piece_cost = 3000 + 1000 * ns;
+// kernel's unit order and its alternating round-robin assignment (item_at).
+long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal,
+                         const SplitCosts& c, int sq, int ns, int grid,
+                         std::vector<long long>& load) {
+  const long long step = c.step, unit_cost = c.unit;
+  const long long piece_cost = c.piece0 + (long long)c.piece_ns * ns;
   load.assign(grid, 0);
   long long pos = 0;
   auto place = [&](long long cost) {
@@ -174,13 +191,16 @@ long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal
 // The split schedule for a problem (none unless it helps by 5% or more in the
 // model above: smaller predicted gains are within the model's error).  Plans
 // are cached: the search walks every candidate.
-SplitPlan split_plan(int units_bh, int S, int causal, int step, int sms, size_t limit) {
+SplitPlan split_plan(int units_bh, int S, int causal, const SplitCosts& costs, int sms,
+                     size_t limit) {
   SplitPlan best;
   const int n_qblocks = (S + 255) / 256, n_kv_tiles = (S + 127) / 128;
   const long long n_items = (long long)units_bh * n_qblocks;
   if (n_items >= (long long)kSplitMaxWaves * sms) return best;
   struct Entry {
-    int units_bh, S, causal, step, sms;
+    int units_bh, S, causal;
+    SplitCosts costs;
+    int sms;
     size_t limit;
     SplitPlan plan;
   };
@@ -189,14 +209,14 @@ SplitPlan split_plan(int units_bh, int S, int causal, int step, int sms, size_t 
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry& e : cache)
-      if (e.units_bh == units_bh && e.S == S && e.causal == causal && e.step == step &&
+      if (e.units_bh == units_bh && e.S == S && e.causal == causal && e.costs == costs &&
           e.sms == sms && e.limit == limit)
         return e.plan;
   }
   std::vector<long long> load;
   const int grid0 = (int)(n_items < sms ? n_items : sms);
   const long long base =
-      split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, step, 0, 1, grid0, load);
+      split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, costs, 0, 1, grid0, load);
   long long best_t = base;
   for (int ns = 2; ns <= 4; ++ns)
     for (int sq = n_qblocks - 1; sq >= 0; --sq) {
@@ -208,7 +228,7 @@ SplitPlan split_plan(int units_bh, int S, int causal, int step, int sms, size_t 
       const long long n_units = n_items + (long long)n_split * (ns - 1);
       const int grid = (int)(n_units < sms ? n_units : sms);
       const long long t =
-          split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, step, sq, ns, grid, load);
+          split_makespan(units_bh, n_qblocks, n_kv_tiles, causal, costs, sq, ns, grid, load);
       if (t < best_t) {
         best_t = t;
         best.split_qb = sq;
@@ -220,7 +240,7 @@ SplitPlan split_plan(int units_bh, int S, int causal, int step, int sms, size_t 
   if (best.n_split_items > 0 && best_t * 100 > base * 95) best = SplitPlan();
   std::lock_guard<std::mutex> lk(mu);
   if (cache.size() >= 64) cache.erase(cache.begin());
-  cache.push_back({units_bh, S, causal, step, sms, limit, best});
+  cache.push_back({units_bh, S, causal, costs, sms, limit, best});
   return best;
 }
 
@@ -237,14 +257,6 @@ unsigned long long next_epoch() {
 bool split_variant(int variant) {
   return variant == ATTN_VARIANT_LEANP || variant == ATTN_VARIANT_BLOCK_EXACT ||
          variant == ATTN_VARIANT_BF16;
-}
-
-// The model's time per key tile of both query tiles (ns at about 2 GHz): the
-// fitted Lean-P figure, scaled by the measured throughput of the MLA shape
-// and of the BF16 path relative to Lean-P at head dim 128.
-int split_step(int variant, int Dqk) {
-  if (variant == ATTN_VARIANT_BF16) return 1500;
-  return Dqk == 192 ? 1140 : 950;
 }
 
 int run(int variant, const void* q, const void* k, const void* v, const float* dq, const float* dk,
@@ -323,7 +335,7 @@ int run(int variant, const void* q, const void* k, const void* v, const float* d
   // key block alone, in the plain (unchunked) item order.
   SplitPlan plan;
   if (workspace && split_variant(variant) && p.chunk_q == B * Hq)
-    plan = split_plan(B * Hq, S, causal, split_step(variant, Dqk), sms, kSplitMaxBytes);
+    plan = split_plan(B * Hq, S, causal, split_costs(variant, Dqk), sms, kSplitMaxBytes);
   if (plan.n_split_items > 0 && workspace_bytes < plan.ws_bytes) return ATTN_ERR_INVALID_ARG;
   p.split_qb = plan.split_qb;
   p.split_ns = plan.ns;
@@ -447,7 +459,7 @@ int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int
   int sms = 0;
   const int st = device_check(&sms);
   if (st != ATTN_OK) return st;
-  *bytes = split_plan(B * Hq, S, causal, split_step(variant, Dqk), sms, kSplitMaxBytes).ws_bytes;
+  *bytes = split_plan(B * Hq, S, causal, split_costs(variant, Dqk), sms, kSplitMaxBytes).ws_bytes;
   return ATTN_OK;
 }
 
