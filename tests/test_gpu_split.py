@@ -318,3 +318,15 @@ def test_bf16_split_against_fp64_and_whole_items(name):
     emul, _, _ = oracle.attention("bf16", case.q, case.k, case.v, rows=rows, causal=causal)
     vmax = float(np.max(np.abs(oracle.bf16_decode(case.v))))
     check_rows(got, emul, np.zeros(len(rows)), vmax)
+
+
+@pytest.mark.parametrize("variant", [fa.ATTN_VARIANT_LEANP, fa.ATTN_VARIANT_BF16], ids=["leanp", "bf16"])
+def test_planner_declines_one_thousand_keys(variant):
+    """At 1K keys every forced plan measured slower than whole items on GB300
+    (1, 4, 8 and 16 heads, causal and not), so the plan model, with the fitted
+    costs of each path, must choose no split there; at 2K keys and few heads
+    it must split."""
+    for H, causal in ((1, True), (4, True), (16, True), (8, False)):
+        assert fa.workspace_size(variant, 1, H, H, 1024, 128, 128, causal) == 0, (H, causal)
+    for H in (1, 2, 4):
+        assert fa.workspace_size(variant, 1, H, H, 2048, 128, 128, True) > 0, H
