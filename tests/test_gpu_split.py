@@ -330,3 +330,26 @@ def test_planner_declines_one_thousand_keys(variant):
         assert fa.workspace_size(variant, 1, H, H, 1024, 128, 128, causal) == 0, (H, causal)
     for H in (1, 2, 4):
         assert fa.workspace_size(variant, 1, H, H, 2048, 128, 128, True) > 0, H
+
+
+@SCHED_VARIANTS
+def test_split_calls_on_two_streams_with_their_own_workspaces(variant):
+    """Calls on different streams may run at the same time, each with its own
+    workspace: every result equals the same call made alone."""
+    case_a, args_a, _, causal_a = make_for(variant, "h8_s2048", 610)
+    case_b, args_b, _, causal_b = make_for(variant, "h2_s4096", 615)
+    want_a = call(variant, args_a, causal_a)
+    want_b = call(variant, args_b, causal_b)
+    torch.cuda.synchronize()
+    ws = [torch.empty(fa.workspace_size(variant, *c.shape, ca), dtype=torch.uint8, device="cuda")
+          for c, ca in ((case_a, causal_a), (case_b, causal_b))]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    got = []
+    for _ in range(3):
+        for s, w, args, ca in zip(streams, ws, (args_a, args_b), (causal_a, causal_b)):
+            with torch.cuda.stream(s):
+                got.append(call(variant, args, ca, workspace=w))
+    torch.cuda.synchronize()
+    for i, (o, l) in enumerate(got):
+        want = want_a if i % 2 == 0 else want_b
+        assert torch.equal(o, want[0]) and torch.equal(l, want[1]), i
