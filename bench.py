@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3940897536,
-                    "sources_sha256": "8ba954e68fd78c7909d91adf50d3e2ef5d810a038c4224ad0d944c9ca263fbfa"}
+PROFILED_TRAFFIC = {"bytes": 3956301824,
+                    "sources_sha256": "0d9b4a7aeb2097e2766eb3dcd9596799e72ee42fc1923aa39f90e4bbf5dbf579"}
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

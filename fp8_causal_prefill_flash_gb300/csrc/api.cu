@@ -133,11 +133,13 @@ size_t split_ws_bytes(int n_split_items, int ns) {
 // The plan model's costs (ns at about 2 GHz): per key tile of both query
 // tiles, per unit (the item boundary), and per piece piece0 + piece_ns * ns
 // (its partial result written, and the ns partial results read and added up
-// by the last piece).
+// by the last piece); and the smallest predicted gain, in percent, for which
+// a split is taken.
 struct SplitCosts {
-  int step, unit, piece0, piece_ns;
+  int step, unit, piece0, piece_ns, min_gain_pct;
   bool operator==(const SplitCosts& o) const {
-    return step == o.step && unit == o.unit && piece0 == o.piece0 && piece_ns == o.piece_ns;
+    return step == o.step && unit == o.unit && piece0 == o.piece0 && piece_ns == o.piece_ns &&
+           min_gain_pct == o.min_gain_pct;
   }
 };
 
@@ -146,10 +148,15 @@ struct SplitCosts {
 // and 192, within 8% of each with 5 us for the launch; the MLA shape's step
 // is the head-dim-128 step scaled by its measured throughput.  BF16: 180
 // plans on 1 to 16 heads, 1K to 16K keys, causal and not, within 7.4% of each
-// with 3 us for the launch.
+// with 3 us for the launch.  The model was fitted with the inputs in L2; with
+// L2 flushed before every call it predicts too much gain, most at 2K keys.
+// The thresholds are the smallest predicted gains above which every plan the
+// model chose, over 75 shapes (1 to 16 heads, 1K to 16K keys, causal and
+// not, GQA), ran at 99% or more of the whole-item speed with L2 flushed: 15%
+// for FP8 (below it, losses of up to 7.5%), 8% for BF16.
 SplitCosts split_costs(int variant, int Dqk) {
-  if (variant == ATTN_VARIANT_BF16) return {1580, 6640, 5360, 1300};
-  return {Dqk == 192 ? 1140 : 950, 5000, 3000, 1000};
+  if (variant == ATTN_VARIANT_BF16) return {1580, 6640, 5360, 1300, 8};
+  return {Dqk == 192 ? 1140 : 950, 5000, 3000, 1000, 15};
 }
 
 // Estimated finishing time of the busiest CTA (ns) when the items of query
@@ -188,9 +195,9 @@ long long split_makespan(int units_bh, int n_qblocks, int n_kv_tiles, int causal
   return m;
 }
 
-// The split schedule for a problem (none unless it helps by 5% or more in the
-// model above: smaller predicted gains are within the model's error).  Plans
-// are cached: the search walks every candidate.
+// The split schedule for a problem (none unless the model above predicts at
+// least the path's minimum gain: smaller predicted gains are within the
+// model's error).  Plans are cached: the search walks every candidate.
 SplitPlan split_plan(int units_bh, int S, int causal, const SplitCosts& costs, int sms,
                      size_t limit) {
   SplitPlan best;
@@ -237,7 +244,8 @@ SplitPlan split_plan(int units_bh, int S, int causal, const SplitCosts& costs, i
         best.ws_bytes = bytes;
       }
     }
-  if (best.n_split_items > 0 && best_t * 100 > base * 95) best = SplitPlan();
+  if (best.n_split_items > 0 && best_t * (100 + costs.min_gain_pct) > base * 100)
+    best = SplitPlan();
   std::lock_guard<std::mutex> lk(mu);
   if (cache.size() >= 64) cache.erase(cache.begin());
   cache.push_back({units_bh, S, causal, costs, sms, limit, best});

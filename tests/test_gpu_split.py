@@ -42,7 +42,7 @@ PATH = {fa.ATTN_VARIANT_LEANP: "leanp", fa.ATTN_VARIANT_BLOCK_EXACT: "variant_e"
 # (B, Hq, Hkv, S, Dqk, causal, per-(batch, kv head) descales)
 SHAPES = {
     "h8_s2048": (1, 8, 8, 2048, 128, True, False),
-    "gqa_b2_ragged": (2, 8, 2, 1500, 128, True, False),
+    "gqa_b2_ragged": (2, 4, 2, 2000, 128, True, False),
     "noncausal_h4": (1, 4, 4, 2000, 128, False, False),
     "mla_h4": (1, 4, 4, 2048, 192, True, False),
     "h2_s4096": (1, 2, 2, 4096, 128, True, False),
@@ -185,6 +185,7 @@ def test_split_bf16_output_is_the_fp32_output_rounded(name, variant):
     TMA stores as a whole item (direct stores for BF16); the values are the
     fp32 output rounded."""
     case, args, _, causal = make_for(variant, name, 560)
+    assert fa.workspace_size(variant, *case.shape, causal) > 0
     f32, _ = call(variant, args, causal)
     b16, _ = call(variant, args, causal, out_dtype=fa.ATTN_OUT_BF16)
     torch.cuda.synchronize()
@@ -196,6 +197,7 @@ def test_split_bf16_output_is_the_fp32_output_rounded(name, variant):
 def test_split_writes_every_output_element_and_nothing_else(out_dtype, variant):
     case, args, _, causal = make_for(variant, "gqa_b2_ragged", 580)
     B, Hq, Hkv, S, Dqk, Dv = case.shape
+    assert fa.workspace_size(variant, *case.shape, causal) > 0
     esz = 4 if out_dtype == fa.ATTN_OUT_F32 else 2
     n_out = B * S * Hq * Dv * esz
     pad = 4096
@@ -280,7 +282,7 @@ def test_split_kernel_reports_a_stall_and_the_next_call_is_correct(variant):
 # one rounding step, 2^-8, and the gate against fp64 (5e-3) still applies.
 BF16_SHAPES = {
     "h8_s2048": (1, 8, 8, 2048, True),
-    "gqa_b2_ragged": (2, 8, 2, 1500, True),
+    "gqa_b2_ragged": (2, 4, 2, 2000, True),
     "noncausal_h4": (1, 4, 4, 2000, False),
     "h2_s4096": (1, 2, 2, 4096, True),
 }

@@ -87,7 +87,7 @@ def check_against_existing(case, q, k, v, d, got):
     check_rows(np.stack([gg[b, i, h] for b, h, i in rows]), want, amb, vmax, tol=2e-3 + 2.0 ** -9)
 
 
-@pytest.mark.parametrize("shape", [(1, 8, 8, 2048), (2, 8, 2, 1500), (1, 32, 32, 2048)],
+@pytest.mark.parametrize("shape", [(1, 8, 8, 2048), (2, 4, 2, 2000), (1, 32, 32, 2048)],
                          ids=["splits", "splits_gqa_ragged", "whole_items"])
 def test_two_calls_in_a_row_match_the_existing_entry_points(lib, shape):
     B, Hq, Hkv, S = shape
