@@ -711,7 +711,7 @@ def split_leg(torch, fa, wl, dev, peaks, n, bf16=False):
 ONLY_PATHS = {"leanp": "fp8_h32_s32k_d128", "exact_fp8": "fp8_h32_s32k_d128",
               "leanp_a3": "fp8_h32_s32k_d128",
               "block_exact": "fp8_h32_s32k_d128", "bf16": "bf16_gqa_h32_8_s16k_d128",
-              "leanp_split": "fp8_h4_s8k_d128",
+              "leanp_split": "fp8_h4_s8k_d128", "bf16_split": "bf16_h4_s8k_d128",
               "quantize": "quantize_bf16_s32k_h32_d128",
               "quantize_hadamard": "quantize_bf16_s32k_h32_d128"}
 
@@ -757,10 +757,17 @@ def run_only(args):
     case = wl.make_case(name, S=args.S)
     B, Hq, Hkv, S, Dqk, Dv = case.shape
     out = torch.empty((B, S, Hq, Dv), dtype=torch.bfloat16, device=dev)
-    if args.only == "bf16":
+    if args.only in ("bf16", "bf16_split"):
         q, k, v = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
                    for a in (case.q, case.k, case.v))
-        fn = lambda: fa.attn_fwd_bf16(q, k, v, out=out)
+        if args.only == "bf16":
+            fn = lambda: fa.attn_fwd_bf16(q, k, v, out=out)
+        else:
+            # the split schedule (few work items), its workspace allocated once
+            need = fa.workspace_size(fa.ATTN_VARIANT_BF16, B, Hq, Hkv, S, Dqk, Dv, True)
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            fn = lambda: fa.attn_fwd_full(fa.ATTN_VARIANT_BF16, q, k, v, out=out,
+                                          workspace=ws if need else None)
     else:
         q, k, v = (torch.from_numpy(a).to(dev) for a in (case.q, case.k, case.v))
         d = [torch.tensor([x], dtype=torch.float32, device=dev) for x in (case.dq, case.dk, case.dv)]
