@@ -92,6 +92,13 @@ class Protocol:
     order_pv: bool = False
     qk_go: int = 4
     split_pv: bool = False
+    # a variant measured on the GPU and not kept (the softmax compiled
+    # slower): softmax 0 starts its epilogue only after tile 1 has written the
+    # item's last P; softmax 1 arrives on p1_last after its last P of an item
+    epi_after_p1: bool = False
+    # planted mistake: the same wait as a parity wait on p_full1, which can be
+    # two phases ahead when tile 1 has two more key tiles to go
+    epi_wait_on_p_full1: bool = False
     # planted mistakes, for the tests that show the checker finds them
     skip_drain_wait: bool = False
     skip_o_done_wait: bool = False
@@ -139,6 +146,7 @@ class Model:
             **{f"p_half{t}": B(f"p_half{t}", 1) for t in range(2)},
             **{f"o_done{t}": B(f"o_done{t}", 1) for t in range(2)},
             **{f"o_free{t}": B(f"o_free{t}", 1) for t in range(2)},
+            "p1_last": B("p1_last", 1),
             **{f"qk_go{t}_{i}": B(f"qk_go{t}_{i}", 1) for t in range(2) for i in range(proto.qk_go)},
             **{f"drain_{r}": B(f"drain_{r}", 1) for r in ("qk", "pv0", "pv1")},
         }
@@ -294,6 +302,7 @@ class Model:
 
     def _softmax(self, t):
         s_cnt = o_cnt = 0
+        p1_cnt = 0  # tile 1's P writes up to this item (counted by softmax 0)
         for item in range(len(self.items)):
             nk = self._nk(item, t)
             for j in range(nk):
@@ -310,7 +319,15 @@ class Model:
                 else:
                     yield ("write_p", t, item, j)
                 yield ("arrive", f"p_full{t}")
+                if self.p.epi_after_p1 and t == 1 and j == nk - 1:
+                    yield ("arrive", "p1_last")
                 o_cnt += 1
+            if self.p.epi_after_p1 and t == 0:
+                if self.p.epi_wait_on_p_full1:
+                    p1_cnt += self._nk(item, 1)
+                    yield _wait("p_full1", p1_cnt - 1)
+                else:
+                    yield _wait("p1_last", item)
             yield _wait(f"o_done{t}", o_cnt - 1)
             yield ("read_o", t, item)
             yield ("arrive", f"o_free{t}")

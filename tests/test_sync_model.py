@@ -4,7 +4,9 @@ schedules with random per-role speeds.
 
 - The protocols the kernel ships show no aliased wait, no deadlock and no data
   race: FP8 unordered with 4 and 3 ring stages, and BF16 ordered with 2
-  stages and four ``qk_go`` barriers per tile.
+  stages and four ``qk_go`` barriers per tile; so do the variants that were
+  built, measured and not kept (two Q buffers, P in halves at head dim 128,
+  tile 0's epilogue held back until tile 1's last P).
 - Mistakes planted in the model are found: two ``qk_go`` barriers per tile
   alias (a first GPU build of that variant ended some launches on the bounded
   wait's timeout), and dropping the S-drain, P.V-done or Q-empty wait is an
@@ -34,8 +36,9 @@ SEEDS = range(400)
     sm.Protocol(stages=3, p_halves=True),                # FP8 Dqk 192, P in two halves
     sm.Protocol(stages=4, order_pv=True, qk_go=4),       # the order with a deeper ring
     sm.Protocol(stages=4, order_pv=True, qk_go=4, split_pv=True),
+    sm.Protocol(stages=4, q_bufs=1, epi_after_p1=True),  # tile 0's epilogue after P1 (not kept)
 ], ids=["fp8", "fp8_mla", "bf16", "fp8_two_q", "fp8_halves", "fp8_mla_halves",
-        "ordered_4stages", "ordered_split"])
+        "ordered_4stages", "ordered_split", "fp8_epi_after_p1"])
 def test_kernel_protocols_have_no_race_or_aliasing(proto):
     assert sm.check(proto, SEEDS) is None
 
@@ -50,6 +53,14 @@ def test_three_ordering_barriers_suffice():
     # the bound in the kernel's argument: S_t(n+3) already needs the P.V product
     # that consumes arrival n; the kernel takes four, a power of two
     assert sm.check(sm.Protocol(stages=2, order_pv=True, qk_go=3), SEEDS) is None
+
+
+def test_epilogue_wait_on_the_p_barrier_aliases():
+    # softmax 0 may reach its epilogue while tile 1 has two more P writes to
+    # go, so a parity wait on p_full1 for the last one is ambiguous; the
+    # variant as built waited on p1_last, one phase per item
+    found = sm.check(sm.Protocol(epi_after_p1=True, epi_wait_on_p_full1=True), SEEDS)
+    assert found is not None and "parity wait cannot tell" in found[2], found
 
 
 def test_missing_drain_wait_is_an_overwrite_of_s():
@@ -87,11 +98,12 @@ def test_model_reports_a_deadlock():
 
 @pytest.mark.parametrize("proto", [
     sm.Protocol(stages=4, q_bufs=1, inject_timeout=True),
+    sm.Protocol(stages=4, q_bufs=1, epi_after_p1=True, inject_timeout=True),
     sm.Protocol(stages=4, q_bufs=2, inject_timeout=True),
     sm.Protocol(stages=4, p_halves=True, inject_timeout=True),
     sm.Protocol(stages=3, q_bufs=1, inject_timeout=True),
     sm.Protocol(stages=2, q_bufs=1, order_pv=True, inject_timeout=True),
-], ids=["fp8", "fp8_two_q", "fp8_halves", "fp8_mla", "bf16"])
+], ids=["fp8", "fp8_epi_after_p1", "fp8_two_q", "fp8_halves", "fp8_mla", "bf16"])
 def test_a_timed_out_wait_leaves_nothing_in_flight(proto):
     assert sm.check(proto, range(600)) is None
 
