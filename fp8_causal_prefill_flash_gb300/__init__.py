@@ -84,10 +84,13 @@ def _open(path):
     lib.attn_fwd_full.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, vp, i, i, i, i, i, i, i, f,
                                   i, vp, vp, sz, vp]
     lib.attn_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(sz)]
+    lib.attn_split_plan.argtypes = [i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(i),
+                                    ctypes.POINTER(i), ctypes.POINTER(sz)]
     lib.attn_debug_timeline.argtypes = [vp, i, i]
     for name in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
                  "attn_quantize_fp8", "attn_fwd_full", "attn_launches_per_call",
-                 "attn_api_version", "attn_debug_timeline", "attn_workspace_size"):
+                 "attn_api_version", "attn_debug_timeline", "attn_workspace_size",
+                 "attn_split_plan"):
         getattr(lib, name).restype = ctypes.c_int
     lib.attn_status_string.argtypes = [i]
     lib.attn_status_string.restype = ctypes.c_char_p
@@ -303,6 +306,19 @@ def workspace_size(variant, B, Hq, Hkv, S, Dqk, Dv, causal=True, flags=0) -> int
                                             int(bool(causal)), int(flags), ctypes.byref(n))
     _raise(st, "attn_workspace_size")
     return int(n.value)
+
+
+def split_plan(variant, B, Hq, Hkv, S, Dqk, Dv, causal, sms, flags=0):
+    """The split schedule ``attn_fwd_full`` would choose on a GPU with ``sms``
+    SMs (``attn_split_plan`` of the C ABI; host only, no device needed):
+    ``(split_qb, ns, bytes)``, ``(0, 1, 0)`` when the problem runs whole
+    items."""
+    qb, ns, n = ctypes.c_int(0), ctypes.c_int(1), ctypes.c_size_t(0)
+    st = load_library().attn_split_plan(int(variant), B, Hq, Hkv, S, Dqk, Dv, int(bool(causal)),
+                                        int(flags), int(sms), ctypes.byref(qb), ctypes.byref(ns),
+                                        ctypes.byref(n))
+    _raise(st, "attn_split_plan")
+    return qb.value, ns.value, n.value
 
 
 def attn_fwd_full(variant, q, k, v, descale_q=None, descale_k=None, descale_v=None, out=None,

@@ -450,25 +450,55 @@ int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
              stream);
 }
 
-int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
-                        int flags, size_t* bytes) {
-  if (!bytes) return ATTN_ERR_INVALID_ARG;
-  *bytes = 0;
+// The split plan attn_fwd_full uses for these arguments on a GPU with `sms`
+// SMs (0: the current device, which must then pass device_check).
+static int plan_query(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                      int flags, int sms, SplitPlan* plan) {
+  *plan = SplitPlan();
   if (variant < ATTN_VARIANT_LEANP || variant > ATTN_VARIANT_LEANP_A3) return ATTN_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || Dqk < 1 || Dv < 1 || Hq % Hkv != 0)
     return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (sms < 0) return ATTN_ERR_INVALID_ARG;
   const long long n_items = (long long)B * Hq * ((S + 255) / 256);
   if (n_items > (1ll << 30) || (long long)B * S > (1ll << 31)) return ATTN_ERR_INVALID_ARG;
   if (!split_variant(variant) || (flags & ATTN_FLAG_TEST_CHUNK_UNITS)) return ATTN_OK;
   // only the unchunked item order splits (see run)
   const size_t kv_unit = (size_t)S * (size_t)(Dqk + Dv) * (variant == ATTN_VARIANT_BF16 ? 2 : 1);
   if (kv_unit * (size_t)((long long)B * Hkv) > kChunkAllBytes) return ATTN_OK;
-  int sms = 0;
-  const int st = device_check(&sms);
-  if (st != ATTN_OK) return st;
-  *bytes = split_plan(B * Hq, S, causal, split_costs(variant, Dqk), sms, kSplitMaxBytes).ws_bytes;
+  if (sms == 0) {
+    const int st = device_check(&sms);
+    if (st != ATTN_OK) return st;
+  }
+  *plan = split_plan(B * Hq, S, causal, split_costs(variant, Dqk), sms, kSplitMaxBytes);
   return ATTN_OK;
+}
+
+int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                        int flags, size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  SplitPlan plan;
+  const int st = plan_query(variant, B, Hq, Hkv, S, Dqk, Dv, causal, flags, 0, &plan);
+  if (st == ATTN_OK) *bytes = plan.ws_bytes;
+  return st;
+}
+
+int attn_split_plan(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                    int flags, int sms, int* split_qb, int* ns, size_t* bytes) {
+  if (!split_qb || !ns || !bytes) return ATTN_ERR_INVALID_ARG;
+  *split_qb = 0;
+  *ns = 1;
+  *bytes = 0;
+  if (sms < 1) return ATTN_ERR_INVALID_ARG;
+  SplitPlan plan;
+  const int st = plan_query(variant, B, Hq, Hkv, S, Dqk, Dv, causal, flags, sms, &plan);
+  if (st == ATTN_OK && plan.n_split_items > 0) {
+    *split_qb = plan.split_qb;
+    *ns = plan.ns;
+    *bytes = plan.ws_bytes;
+  }
+  return st;
 }
 
 const char* attn_status_string(int status) {

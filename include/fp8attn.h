@@ -76,7 +76,7 @@
 extern "C" {
 #endif
 
-#define FP8ATTN_API_VERSION 8
+#define FP8ATTN_API_VERSION 9
 
 /* Return codes of every entry point. */
 typedef enum {
@@ -238,6 +238,21 @@ int attn_fwd_full(int variant, const void* q, const void* k, const void* v,
  */
 int attn_workspace_size(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
                         int flags, size_t* bytes);
+
+/*
+ * The split schedule that attn_fwd_full would choose for these arguments on
+ * a GPU with `sms` SMs (>= 1), computed on the host without touching any
+ * device: the items of query blocks >= *split_qb (256 query rows each) run
+ * in *ns pieces, with *bytes of workspace; *ns = 1, *split_qb = 0 and
+ * *bytes = 0 when the problem runs whole items.  For capacity planning and
+ * for testing the schedule's choices.  This query has no counterpart in the
+ * articles, and neither has the split schedule it describes.  Returns an
+ * attn_status (ATTN_ERR_INVALID_ARG for invalid arguments, a NULL output
+ * pointer or sms < 1); on error the non-NULL outputs hold the no-split
+ * values.
+ */
+int attn_split_plan(int variant, int B, int Hq, int Hkv, int S, int Dqk, int Dv, int causal,
+                    int flags, int sms, int* split_qb, int* ns, size_t* bytes);
 
 /* Input element type for attn_quantize_fp8. */
 typedef enum { ATTN_IN_BF16 = 0, ATTN_IN_F32 = 1 } attn_in_dtype;

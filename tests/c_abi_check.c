@@ -57,6 +57,18 @@ int main(void) {
     fprintf(stderr, "library and header versions differ\n");
     return 1;
   }
+  /* the split schedule, from the host alone: 4 heads at 8K keys on 152 SMs
+   * split their last 13 query blocks in two */
+  {
+    int qb = -1, ns = -1;
+    size_t nb = 0;
+    if (attn_split_plan(ATTN_VARIANT_LEANP, 1, 4, 4, 8192, 128, 128, 1, 0, 152, &qb, &ns, &nb) !=
+            ATTN_OK ||
+        qb != 19 || ns != 2 || nb == 0) {
+      fprintf(stderr, "attn_split_plan: %d %d %zu\n", qb, ns, nb);
+      return 1;
+    }
+  }
 
   uint8_t *hq = malloc(nq), *hk = malloc(nk), *hv = malloc(nk);
   uint16_t* hout = malloc(nq * 2);

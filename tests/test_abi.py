@@ -19,14 +19,14 @@ def test_header_declares_the_entry_points():
     for n in ("attn_fwd_fp8", "attn_fwd_fp8_exact", "attn_fwd_bf16", "attn_fwd_ex",
               "attn_quantize_fp8", "attn_fwd_full", "attn_status_string",
               "attn_launches_per_call", "attn_api_version", "attn_debug_timeline",
-              "attn_workspace_size"):
+              "attn_workspace_size", "attn_split_plan"):
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for n in fa.declared_functions():
         assert hasattr(lib, n), n
-    assert lib.attn_api_version() == 8
+    assert lib.attn_api_version() == 9
     assert lib.attn_launches_per_call() == 1
 
 
