@@ -82,6 +82,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # with: for any other sources the bench reports null.
 PROFILED_TRAFFIC = {"bytes": 3956301824,
                     "sources_sha256": "0d9b4a7aeb2097e2766eb3dcd9596799e72ee42fc1923aa39f90e4bbf5dbf579"}
+# (the kernel, its PTX helpers and its launch; the host-only split planner in
+# split_plan.h does not touch the whole-item launch and is not part of the key)
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/ptx.cuh",
                   "fp8_causal_prefill_flash_gb300/csrc/api.cu")

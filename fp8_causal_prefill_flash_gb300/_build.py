@@ -12,7 +12,8 @@ SO = os.path.join(PKG, "libfp8attn.so")
 # debug build with the clock64 role timeline (attn_debug_timeline)
 SO_TIMELINE = os.path.join(PKG, "libfp8attn_timeline.so")
 SOURCES = [os.path.join(CSRC, "api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd.cuh", "ptx.cuh", "quant.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd.cuh", "ptx.cuh", "quant.cuh",
+                                                   "split_plan.h")] + [
     os.path.join(ROOT, "include", "fp8attn.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
