@@ -80,8 +80,8 @@ def job_tflops(flops_per_rank, world, ms_max):
 # capture (dram__bytes_read.sum + dram__bytes_write.sum; profiles/ has the
 # summary and the command).  It belongs to the kernel sources it was taken
 # with: for any other sources the bench reports null.
-PROFILED_TRAFFIC = {"bytes": 3956301824,
-                    "sources_sha256": "0d9b4a7aeb2097e2766eb3dcd9596799e72ee42fc1923aa39f90e4bbf5dbf579"}
+PROFILED_TRAFFIC = {"bytes": 3951305216,
+                    "sources_sha256": "2c0543fb1e52dfcebee2e8a494b84e0e9945b325b0108f8bcc904c0c1700463d"}
 # (the kernel, its PTX helpers and its launch; the host-only split planner in
 # split_plan.h does not touch the whole-item launch and is not part of the key)
 KERNEL_SOURCES = ("fp8_causal_prefill_flash_gb300/csrc/attn_fwd.cuh",
